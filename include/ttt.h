@@ -1,0 +1,142 @@
+/*
+ * ttt.h -- C ABI of libttt: the TTT-E2E inner-loop (test-time training) prefill
+ * on one B300 GPU.
+ *
+ * The operation (pages "把 Transformer 做成“终身学习者”：TTT-E2E 如何让大模型边用边学？",
+ * §4.2 "推理阶段（Inner Loop 复用）" and §4.4 "伪代码"; "TTT-E2E技术：突破大语言模型上下文限制的新范式",
+ * §2.1 "参数更新机制"): text is fed chunk by chunk; for each chunk of at most b
+ * tokens a decoder-only Transformer with sliding-window attention (window k,
+ * k >= b) runs forward, the mean next-token cross-entropy over the chunk is
+ * taken, the loss is backpropagated through the last quarter of the blocks
+ * only, and one SGD step W <- W - eta*dW is applied to the MLP weights
+ * (W_up, W_down) of those blocks -- the "fast weights" -- before the next chunk.
+ * The key/value cache keeps only the last k positions per layer.
+ *
+ * Model: pre-norm blocks h = x + Attn(RMSNorm(x)), y = h + GELU_tanh(RMSNorm(h).W_up).W_down,
+ * logits = RMSNorm(x_L).W_lm; multi-head attention with rotate-half RoPE
+ * (inv_freq_i = theta^(-2i/d_head), absolute positions from 0), scale
+ * 1/sqrt(d_head), query p sees keys j with p - k < j <= p; no biases.
+ *
+ * Ownership: the context owns all device memory.  Host pointers passed in are
+ * read or written only during the call and never retained.
+ * Streams: all work is enqueued on the stream given to ttt_create.
+ * Errors: every call returns 0 or a negative TTT_ERR_* code; after an error the
+ * context may only be reloaded (ttt_load_weights) or destroyed.
+ */
+#ifndef TTT_H
+#define TTT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define TTT_API __attribute__((visibility("default")))
+#else
+#define TTT_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TTT_OK 0
+#define TTT_ERR_ARG (-1)         /* null pointer, n outside 1..b, token id outside [0, vocab), k < b, ... */
+#define TTT_ERR_UNSUPPORTED (-2) /* a shape this build does not handle (see ttt_create)                 */
+#define TTT_ERR_STATE (-3)       /* prefill before ttt_load_weights                                     */
+#define TTT_ERR_OOM (-4)         /* device allocation failed                                            */
+#define TTT_ERR_CUDA (-5)        /* a CUDA runtime call failed                                          */
+#define TTT_ERR_DEVICE (-6)      /* a kernel reported an error: bounded wait expired or bad token id    */
+
+typedef struct ttt_ctx ttt_ctx;
+
+typedef struct {
+  int32_t n_layers;     /* L                                                        */
+  int32_t n_trainable;  /* S = number of trailing blocks whose MLPs learn; L/4       */
+  int32_t d_model;      /* d                                                        */
+  int32_t n_heads;      /* H; d_head = d / H                                        */
+  int32_t d_ff;         /* MLP hidden width (4d in every shipped workload)          */
+  int32_t vocab;        /* V                                                        */
+  int32_t window;       /* k: a query sees the k most recent positions, itself included */
+  int32_t chunk;        /* b: tokens per inner-loop step, k >= b                    */
+  int32_t n_seqs;       /* independent sequences, each with its own fast weights and cache */
+  double rope_theta;
+  float rms_eps;        /* 1e-6 */
+  float eta;            /* SGD step size of the inner loop */
+  int32_t compute;      /* 0: fp32 (every product as three bf16 products of hi/lo
+                           halves, fp32 accumulate); 1: bf16 operands, fp32
+                           accumulate; fast weights are fp32 in both           */
+} ttt_config;
+
+/*
+ * Create a context on the current CUDA device; work goes to `cuda_stream`
+ * (cudaStream_t, NULL = default stream).
+ * Supported: d_head % 16 == 0 and d_head <= 128 (<= 64 when compute == 0),
+ * d_model % 64 == 0, d_ff % 64 == 0, vocab % 8 == 0, window % 128 == 0,
+ * 1 <= chunk <= window, 1 <= n_trainable <= n_layers.  Otherwise
+ * TTT_ERR_UNSUPPORTED (shape) or TTT_ERR_ARG (inconsistent values).
+ */
+TTT_API int ttt_create(const ttt_config* cfg, void* cuda_stream, ttt_ctx** out);
+
+/*
+ * Copy the fp32 weight blob (host memory, n_floats values) to the device and
+ * reset every sequence: position 0, empty cache, fast weights = the loaded
+ * W_up / W_down of the trainable blocks.  Blob order, all row-major, y = x.W:
+ *   E[V][d];
+ *   for each layer: g_attn[d], Wq[d][d], Wk[d][d], Wv[d][d], Wo[d][d],
+ *                   g_mlp[d], W_up[d][d_ff], W_down[d_ff][d];
+ *   g_final[d]; W_lm[d][V].
+ */
+TTT_API int ttt_load_weights(ttt_ctx* ctx, const float* host_blob, size_t n_floats);
+
+/*
+ * One inner-loop step for every sequence.
+ *   tokens      host int32 [n_seqs][n], the next n tokens of each sequence (1 <= n <= b)
+ *   next_tokens host int32 [n_seqs], the token after the chunk (target of its last
+ *               position), -1 at the end of the sequence
+ *   chunk_loss  host float [n_seqs], out: mean cross-entropy over the chunk's
+ *               valid targets, computed with the fast weights before this step
+ * The fast weights are then updated and the position advances by n.  Blocks
+ * until the losses are on the host.
+ */
+TTT_API int ttt_prefill_chunk(ttt_ctx* ctx, const int32_t* tokens, int32_t n, const int32_t* next_tokens,
+                      float* chunk_loss);
+
+/*
+ * Same step with DEVICE buffers, enqueued on the context stream without any
+ * synchronisation: d_tokens int32 [n_seqs][n], d_next int32 [n_seqs],
+ * d_loss float [n_seqs] (written when the work completes).  Token ids are
+ * checked on the device; a bad id is reported by the next ttt_sync.
+ */
+TTT_API int ttt_prefill_chunk_dev(ttt_ctx* ctx, const int32_t* d_tokens, int32_t n, const int32_t* d_next,
+                          float* d_loss);
+
+/*
+ * Whole sequences with DEVICE buffers: d_tokens int32 [n_seqs][T], d_losses
+ * float [n_seqs][ceil(T/b)].  Equivalent to ceil(T/b) calls of
+ * ttt_prefill_chunk_dev in order (targets run across chunk boundaries; the
+ * last position has none).  Asynchronous like ttt_prefill_chunk_dev.
+ */
+TTT_API int ttt_prefill_sequence_dev(ttt_ctx* ctx, const int32_t* d_tokens, int32_t T, float* d_losses);
+
+/* Wait for the context stream and report a device-side error (TTT_ERR_DEVICE). */
+TTT_API int ttt_sync(ttt_ctx* ctx);
+
+/*
+ * Copy the current fast weights of trainable block `suffix_layer` (0 = block
+ * L-S, ..., S-1 = block L-1) of sequence `seq` to host memory:
+ * w_up float [d][d_ff], w_down float [d_ff][d] (either may be NULL).
+ */
+TTT_API int ttt_get_fast_weights(ttt_ctx* ctx, int32_t seq, int32_t suffix_layer, float* w_up, float* w_down);
+
+/* Current absolute position (tokens consumed) of every sequence. */
+TTT_API int64_t ttt_position(const ttt_ctx* ctx);
+
+TTT_API void ttt_destroy(ttt_ctx* ctx);
+
+/* Text of the last error on this context ("" if none); valid until the next call. */
+TTT_API const char* ttt_last_error(const ttt_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TTT_H */

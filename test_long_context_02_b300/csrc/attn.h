@@ -1,0 +1,46 @@
+// Sliding-window attention kernels (attn_fwd.cu, attn_bwd.cu).
+#pragma once
+#include <cuda.h>
+#include "kernels.h"
+
+namespace ttt {
+
+// Geometry of one chunk's attention for one sequence and layer.  Activations
+// are token-major [rows][d] (head h in columns h*dh .. h*dh+dh-1).
+struct AttnArgs {
+  int n = 0;            // queries = the chunk's own tokens
+  int H = 0, dh = 0;
+  int window = 0;       // k (multiple of 128); also the number of cache slots
+  long pos0 = 0;        // absolute position of the chunk's first token
+  float scale_log2 = 0; // log2(e) / sqrt(dh)
+  bf16* o_hi = nullptr; bf16* o_lo = nullptr; long ldo = 0;   // forward output [n][d]
+  float* lse = nullptr; // [H][n] log2-sum-exp of the scaled scores (optional)
+  int* err = nullptr;
+};
+
+// TMA maps (box {64, 128}) of: queries [n][d]; cache keys/values [k][d];
+// the chunk's own keys/values [n][d].  *_l: the bf16 remainders (split mode).
+struct AttnMaps {
+  CUtensorMap q, ql, kr, krl, vr, vrl, ko, kol, vo, vol;
+};
+
+int attn_fwd_run(const AttnMaps& m, const AttnArgs& a, bool split, cudaStream_t st);
+
+// Backward: geometry from g; lse ([H][n], log2 domain) from the forward;
+// D[h][t] = rowsum(dO * O); outputs dq (all keys) and dk, dv (own keys only),
+// fp32 token-major [n][ldg].
+struct AttnBwdArgs {
+  AttnArgs g;
+  const float* lse = nullptr;
+  const float* D = nullptr;
+  float* dq = nullptr; float* dk = nullptr; float* dv = nullptr; long ldg = 0;
+  float scale = 0.f;  // 1/sqrt(dh)
+};
+struct AttnBwdMaps {
+  AttnMaps f;          // q, cache k/v, own k/v as in the forward
+  CUtensorMap dO, dOl; // output gradient [n][d]
+};
+
+int attn_bwd_run(const AttnBwdMaps& m, const AttnBwdArgs& a, bool split, cudaStream_t st);
+
+}  // namespace ttt

@@ -1,0 +1,427 @@
+// Persistent warp-specialised tcgen05 GEMM with fused epilogues.
+//
+// Every dense contraction of the TTT-E2E inner-loop step runs here: the
+// frozen QKV / O / MLP projections of the forward, the LM head (fused with the
+// vocab-tiled softmax statistics of the cross-entropy and, in the backward,
+// with the logit gradient), the activation-gradient (dX) products of the
+// suffix blocks, and the fast-weight gradients dW = X^T dY whose epilogue
+// applies the SGD step W <- W - eta*dW in place (pages: "把 Transformer 做成
+// “终身学习者”", §4.2, one mini-batch gradient step on the last-quarter MLPs;
+// "测试时训练：长上下文的持续学习", §2.1.2, theta <- theta - eta*grad).
+//
+// CTA = 6 warps: warp 0 issues TMA loads into a ring of shared-memory stages,
+// warp 1 owns the TMEM accumulators and issues tcgen05.mma (single thread),
+// warps 2-5 drain a 128 x BN fp32 accumulator from TMEM (one row per thread)
+// and apply the epilogue while the MMA warp fills the other accumulator.
+// Tiles are 128 x BN x 64 (bf16, 128-byte swizzle); operands are K-major or
+// MN-major per call, so weights stay in one row-major copy for both x.W
+// (MN-major B) and dY.W^T (K-major B), and dW = X^T dY reads activations
+// MN-major without a transpose.  In split mode each operand is a bf16 pair
+// (hi, lo) and every k-step issues hi*hi + hi*lo + lo*hi.
+#include <cstdio>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "tmap.h"
+
+namespace ttt {
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int kSmemBudget = 192 * 1024;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kGeluC = 0.7978845608028654f;  // sqrt(2/pi)
+
+template <int BN, bool SPLIT>
+struct Cfg {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int NOP = SPLIT ? 2 : 1;
+  static constexpr int STAGE = NOP * (A_BYTES + B_BYTES);
+  static constexpr int STAGES = kSmemBudget / STAGE;
+  static constexpr uint32_t TMEM_COLS = 2 * BN;
+  static constexpr int SMEM = STAGES * STAGE + 1024 + 256;
+};
+
+TTT_DEV bool wait_drain(uint64_t* bar, uint32_t parity, int* err) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      if (err) atomicCAS(err, 0, (int)DERR_TIMEOUT_DRAIN);
+      return false;
+    }
+  }
+  return true;
+}
+
+TTT_DEV float gelu_f(float a) { return 0.5f * a * (1.f + tanhf(kGeluC * (a + 0.044715f * a * a * a))); }
+TTT_DEV float gelu_grad_f(float a) {
+  const float t = tanhf(kGeluC * (a + 0.044715f * a * a * a));
+  return 0.5f * (1.f + t) + 0.5f * a * (1.f - t * t) * kGeluC * (1.f + 3.f * 0.044715f * a * a);
+}
+
+// Load one operand tile (rows x 64 of K) for K index k0 and M/N origin r0.
+template <int ROWS>
+TTT_DEV void load_tile(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int r0, int k0, int mn) {
+  if (!mn) {
+    tma_load_2d(dst, map, bar, k0, r0);  // box {64 K, ROWS}
+  } else {
+#pragma unroll
+    for (int j = 0; j < ROWS / 64; ++j) tma_load_2d(dst + j * (BK * 128), map, bar, r0 + 64 * j, k0);  // box {64, 64 K}
+  }
+}
+
+TTT_DEV uint64_t tile_desc(uint32_t base, int kk, int mn) {
+  return mn ? sdesc_sw128(base + kk * 2048, BK * 128, 1024) : sdesc_sw128(base + kk * 32, 16, 1024);
+}
+
+TTT_DEV void store_opnd(bf16* hi, bf16* lo, long off, float v) {
+  bf16 h = __float2bfloat16_rn(v);
+  hi[off] = h;
+  if (lo) lo[off] = __float2bfloat16_rn(v - __bfloat162float(h));
+}
+
+// 32 consecutive values of one row: vector path when the whole fragment is in range.
+TTT_DEV void store_opnd32(bf16* hi, bf16* lo, long base, const float (&v)[32], int ncols) {
+  if (ncols == 32) {
+    uint32_t h[16], l[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      __nv_bfloat162 t = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+      h[i] = *reinterpret_cast<uint32_t*>(&t);
+      if (lo) {
+        float2 f = __bfloat1622float2(t);
+        l[i] = pack_bf16(v[2 * i] - f.x, v[2 * i + 1] - f.y);
+      }
+    }
+    uint4* ph = reinterpret_cast<uint4*>(hi + base);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ph[i] = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+    if (lo) {
+      uint4* pl = reinterpret_cast<uint4*>(lo + base);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) pl[i] = make_uint4(l[4 * i], l[4 * i + 1], l[4 * i + 2], l[4 * i + 3]);
+    }
+  } else {
+    for (int i = 0; i < ncols; ++i) store_opnd(hi, lo, base + i, v[i]);
+  }
+}
+
+TTT_DEV void store_f32_32(float* p, const float (&v)[32], int ncols) {
+  if (ncols == 32) {
+    float4* q = reinterpret_cast<float4*>(p);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+  } else {
+    for (int i = 0; i < ncols; ++i) p[i] = v[i];
+  }
+}
+
+TTT_DEV void load_f32_32(const float* p, float (&v)[32], int ncols) {
+  if (ncols == 32) {
+    const float4* q = reinterpret_cast<const float4*>(p);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float4 t = q[i];
+      v[4 * i] = t.x; v[4 * i + 1] = t.y; v[4 * i + 2] = t.z; v[4 * i + 3] = t.w;
+    }
+  } else {
+    for (int i = 0; i < ncols; ++i) v[i] = p[i];
+  }
+}
+
+template <int BN, bool SPLIT, int EPI>
+__global__ void __launch_bounds__(192, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tAl,
+                const __grid_constant__ CUtensorMap tB, const __grid_constant__ CUtensorMap tBl, const GemmArgs g) {
+  using C = Cfg<BN, SPLIT>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* tfull = empty + C::STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mt = (g.M + BM - 1) / BM, nt = (g.N + BN - 1) / BN, ntiles = mt * nt;
+  const int nk = (g.K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 128);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch(&tA);
+    tma_prefetch(&tB);
+    if (SPLIT) {
+      tma_prefetch(&tAl);
+      tma_prefetch(&tBl);
+    }
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {  // ---------------------------------------------- TMA producer
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      uint32_t issued = 0;  // bit s: stage s has a fill in flight or landed
+      uint32_t iss_par = 0; // bit s: parity of that fill
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        const int m0 = (t % mt) * BM, n0 = (t / mt) * BN;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, g.err, DERR_TIMEOUT_PRODUCER)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + s * C::STAGE;
+          mbar_expect_tx(&full[s], C::STAGE);
+          load_tile<BM>(st, &tA, &full[s], m0, kb * BK, g.a_mn);
+          load_tile<BN>(st + C::A_BYTES, &tB, &full[s], n0, kb * BK, g.b_mn);
+          if (SPLIT) {
+            load_tile<BM>(st + C::A_BYTES + C::B_BYTES, &tAl, &full[s], m0, kb * BK, g.a_mn);
+            load_tile<BN>(st + 2 * C::A_BYTES + C::B_BYTES, &tBl, &full[s], n0, kb * BK, g.b_mn);
+          }
+          issued |= 1u << s;
+          iss_par = (iss_par & ~(1u << s)) | (ph << s);
+          if (++s == C::STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      // no TMA write may still be in flight when the CTA exits
+      for (int i = 0; i < C::STAGES; ++i)
+        if (issued & (1u << i)) wait_drain(&full[i], (iss_par >> i) & 1u, g.err);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // ------------------------------------------------ MMA issuer
+      const uint32_t idesc = idesc_bf16(BM, BN, g.a_mn, g.b_mn);
+      int s = 0;
+      uint32_t ph = 0;
+      int it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++it) {
+        const int buf = it & 1;
+        const uint32_t use = (uint32_t)(it >> 1);
+        if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag, g.err, DERR_TIMEOUT_MMA)) break;
+        tc_fence_after();
+        const uint32_t dt = tmem + (uint32_t)(buf * BN);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&full[s], ph, abort_flag, g.err, DERR_TIMEOUT_MMA)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a = smem_u32(smem + s * C::STAGE);
+          const uint32_t b = a + C::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t da = tile_desc(a, kk, g.a_mn), db = tile_desc(b, kk, g.b_mn);
+            mma_bf16(dt, da, db, idesc, (kb | kk) ? 1u : 0u);
+            if (SPLIT) {
+              const uint64_t dal = tile_desc(a + C::A_BYTES + C::B_BYTES, kk, g.a_mn);
+              const uint64_t dbl = tile_desc(a + 2 * C::A_BYTES + C::B_BYTES, kk, g.b_mn);
+              mma_bf16(dt, da, dbl, idesc, 1u);
+              mma_bf16(dt, dal, db, idesc, 1u);
+            }
+          }
+          mma_commit(&empty[s]);
+          if (++s == C::STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&tfull[buf]);
+      }
+      mma_commit(drain);  // every MMA issued above has finished once this arrives
+      wait_drain(drain, 0, g.err);
+    }
+  } else {  // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    int it = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+      const int buf = it & 1;
+      const uint32_t use = (uint32_t)(it >> 1);
+      const bool got = mbar_wait(&tfull[buf], use & 1u, abort_flag, g.err, DERR_TIMEOUT_EPILOGUE);
+      if (!__all_sync(0xffffffffu, got)) break;  // warp-uniform: tcgen05.ld below is .sync.aligned
+      tc_fence_after();
+      const int mtile = t % mt, ntile = t / mt;
+      const int row = mtile * BM + q * 32 + lane;
+      const int n0 = ntile * BN;
+      const bool rok = row < g.M;
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
+      float ce_m = -INFINITY, ce_s = 0.f;
+      int tg = -1;
+      float lse_r = 0.f;
+      if (EPI == EPI_CE_FWD || EPI == EPI_CE_BWD) {
+        if (rok) tg = g.tgt[row];
+        if (EPI == EPI_CE_BWD && rok) lse_r = g.lse[row];
+        if (EPI == EPI_CE_BWD) ce_s = g.scale_dev ? *g.scale_dev : g.scale;
+      }
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        float v[32];
+        tmem_ld32(taddr + (uint32_t)(c * 32), v);
+        const int c0 = n0 + c * 32;
+        const int ncols = min(32, g.N - c0);
+        if (!rok || ncols <= 0) continue;
+        if (EPI == EPI_F32) {
+          store_f32_32(g.out32 + (long)row * g.ldo32 + c0, v, ncols);
+        } else if (EPI == EPI_OPND) {
+          store_opnd32(g.oh, g.ol, (long)row * g.ldo + c0, v, ncols);
+        } else if (EPI == EPI_RESID) {
+          float r[32];
+          load_f32_32(g.resid + (long)row * g.ldr + c0, r, ncols);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] += v[i];
+          store_f32_32(g.out32 + (long)row * g.ldo32 + c0, r, ncols);
+        } else if (EPI == EPI_GELU) {
+          store_f32_32(g.out32 + (long)row * g.ldo32 + c0, v, ncols);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = gelu_f(v[i]);
+          store_opnd32(g.oh, g.ol, (long)row * g.ldo + c0, v, ncols);
+        } else if (EPI == EPI_GELU_BWD) {
+          float a[32];
+          load_f32_32(g.aux + (long)row * g.ldaux + c0, a, ncols);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] *= gelu_grad_f(a[i]);
+          store_opnd32(g.oh, g.ol, (long)row * g.ldo + c0, v, ncols);
+        } else if (EPI == EPI_SGD) {
+          float w[32];
+          float* wp = g.w32 + (long)row * g.ldw + c0;
+          load_f32_32(wp, w, ncols);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) w[i] -= g.eta * v[i];
+          store_f32_32(wp, w, ncols);
+          store_opnd32(g.wh, g.wl, (long)row * g.ldw + c0, w, ncols);
+        } else if (EPI == EPI_CE_FWD) {
+          float mx = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (i < ncols) mx = fmaxf(mx, v[i]);
+          const float mn = fmaxf(ce_m, mx);
+          float s = 0.f;
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (i < ncols) s += exp2f((v[i] - mn) * kLog2e);
+          ce_s = ce_s * exp2f((ce_m - mn) * kLog2e) + s;
+          ce_m = mn;
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (c0 + i == tg) g.zt[row] = v[i];
+        } else if (EPI == EPI_CE_BWD) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float p = exp2f((v[i] - lse_r) * kLog2e);
+            v[i] = (tg >= 0) ? (p - ((c0 + i == tg) ? 1.f : 0.f)) * ce_s : 0.f;
+          }
+          store_opnd32(g.oh, g.ol, (long)row * g.ldo + c0, v, ncols);
+        }
+      }
+      if (EPI == EPI_CE_FWD && rok) g.part[(long)ntile * g.M + row] = make_float2(ce_m, ce_s);
+      tc_fence_before();
+      mbar_arrive(&tempty[buf]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+// Operand rows along M (or N) = `rows`, reduction length K.
+bool operand_map(CUtensorMap* m, const bf16* p, const Opnd& o, int rows, int K, int box_rows) {
+  if (!o.mn) return make_map(m, p, (uint64_t)K, (uint64_t)rows, (uint64_t)o.ld, (uint32_t)box_rows);
+  return make_map(m, p, (uint64_t)rows, (uint64_t)K, (uint64_t)o.ld, 64u);
+}
+
+template <int BN, bool SPLIT, int EPI>
+int launch(const CUtensorMap& a, const CUtensorMap& al, const CUtensorMap& b, const CUtensorMap& bl,
+           const GemmArgs& g, cudaStream_t st) {
+  using C = Cfg<BN, SPLIT>;
+  auto kern = gemm_kernel<BN, SPLIT, EPI>;
+  static bool attr_set = false;  // per instantiation
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return (int)e;
+    attr_set = true;
+  }
+  const int tiles = ((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN);
+  const int grid = tiles < num_sms() ? tiles : num_sms();
+  kern<<<grid, 192, C::SMEM, st>>>(a, al, b, bl, g);
+  return (int)cudaGetLastError();
+}
+
+template <int BN, bool SPLIT>
+int dispatch_epi(int epi, const CUtensorMap& a, const CUtensorMap& al, const CUtensorMap& b,
+                 const CUtensorMap& bl, const GemmArgs& g, cudaStream_t st) {
+  switch (epi) {
+    case EPI_F32: return launch<BN, SPLIT, EPI_F32>(a, al, b, bl, g, st);
+    case EPI_OPND: return launch<BN, SPLIT, EPI_OPND>(a, al, b, bl, g, st);
+    case EPI_RESID: return launch<BN, SPLIT, EPI_RESID>(a, al, b, bl, g, st);
+    case EPI_GELU: return launch<BN, SPLIT, EPI_GELU>(a, al, b, bl, g, st);
+    case EPI_GELU_BWD: return launch<BN, SPLIT, EPI_GELU_BWD>(a, al, b, bl, g, st);
+    case EPI_SGD: return launch<BN, SPLIT, EPI_SGD>(a, al, b, bl, g, st);
+    case EPI_CE_FWD: return launch<BN, SPLIT, EPI_CE_FWD>(a, al, b, bl, g, st);
+    case EPI_CE_BWD: return launch<BN, SPLIT, EPI_CE_BWD>(a, al, b, bl, g, st);
+  }
+  return (int)cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+// Tile width for N: the one that needs the fewest tile-columns of work per SM
+// (waves x BN), preferring the wider tile on a tie.
+int pick_bn(int M, int N) {
+  const int sms = num_sms();
+  const int mt = (M + BM - 1) / BM;
+  const long t256 = (long)mt * ((N + 255) / 256), t128 = (long)mt * ((N + 127) / 128);
+  const long c256 = ((t256 + sms - 1) / sms) * 256, c128 = ((t128 + sms - 1) / sms) * 128;
+  return (N <= 128 || c128 < c256) ? 128 : 256;
+}
+
+int gemm_run(int epi, const Opnd& A, const Opnd& B, GemmArgs g, bool split, cudaStream_t st) {
+  if (g.M <= 0 || g.N <= 0 || g.K <= 0) return 0;
+  if (epi < 0 || epi >= EPI_COUNT) return (int)cudaErrorInvalidValue;
+  if (split && (!A.lo || !B.lo)) return (int)cudaErrorInvalidValue;
+  g.a_mn = A.mn;
+  g.b_mn = B.mn;
+  const int bn = pick_bn(g.M, g.N);
+  CUtensorMap a, al, b, bl;
+  if (!operand_map(&a, A.hi, A, g.M, g.K, BM) || !operand_map(&b, B.hi, B, g.N, g.K, bn))
+    return (int)cudaErrorInvalidValue;
+  al = a;
+  bl = b;
+  if (split && (!operand_map(&al, A.lo, A, g.M, g.K, BM) || !operand_map(&bl, B.lo, B, g.N, g.K, bn)))
+    return (int)cudaErrorInvalidValue;
+  if (bn == 128)
+    return split ? dispatch_epi<128, true>(epi, a, al, b, bl, g, st) : dispatch_epi<128, false>(epi, a, al, b, bl, g, st);
+  return split ? dispatch_epi<256, true>(epi, a, al, b, bl, g, st) : dispatch_epi<256, false>(epi, a, al, b, bl, g, st);
+}
+
+}  // namespace ttt

@@ -1,0 +1,55 @@
+// Internal C++ interface between the host orchestrator and the CUDA kernels.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+namespace ttt {
+
+using bf16 = __nv_bfloat16;
+
+// ------------------------------------------------------------------ GEMM
+// C[M,N] = A[M,K] . B[N,K]^T on tcgen05 (bf16 operands, fp32 accumulate in
+// TMEM), followed by one of these epilogues on each fp32 accumulator value.
+enum Epi : int {
+  EPI_F32 = 0,      // out32 = acc
+  EPI_OPND = 1,     // (oh, ol) = split(acc)                 -> next GEMM operand
+  EPI_RESID = 2,    // out32 = resid + acc                   (residual stream)
+  EPI_GELU = 3,     // out32 = acc ; (oh, ol) = gelu_tanh(acc)
+  EPI_GELU_BWD = 4, // (oh, ol) = acc * gelu_tanh'(aux)
+  EPI_SGD = 5,      // w32 -= eta*acc ; (wh, wl) = split(w32)  (fused SGD step)
+  EPI_CE_FWD = 6,   // per (row, N-tile): (max, sum exp) of logits; zt[row] = logit of target
+  EPI_CE_BWD = 7,   // (oh, ol) = (softmax(acc) - onehot(tgt)) * scale, softmax from lse
+  EPI_COUNT = 8
+};
+
+struct GemmArgs {
+  int M = 0, N = 0, K = 0;
+  int a_mn = 0, b_mn = 0;
+  float* out32 = nullptr; long ldo32 = 0;
+  bf16* oh = nullptr; bf16* ol = nullptr; long ldo = 0;
+  const float* resid = nullptr; long ldr = 0;
+  const float* aux = nullptr; long ldaux = 0;
+  float* w32 = nullptr; bf16* wh = nullptr; bf16* wl = nullptr; long ldw = 0; float eta = 0.f;
+  const int* tgt = nullptr; float2* part = nullptr; float* zt = nullptr; const float* lse = nullptr;
+  float scale = 0.f;
+  const float* scale_dev = nullptr;  // CE_BWD: device copy of the scale (used when non-null)
+  int* err = nullptr;
+};
+
+// One GEMM operand in HBM.  K-major: row-major [rows][ld] holding the K index
+// in its columns.  MN-major: row-major [K][ld] holding the M (or N) index in
+// its columns.  lo is the bf16 remainder of the fp32 value (split mode) or null.
+struct Opnd {
+  const bf16* hi = nullptr;
+  const bf16* lo = nullptr;
+  long ld = 0;
+  int mn = 0;
+};
+
+// Returns 0 or a cudaError_t value.
+int gemm_run(int epi, const Opnd& A, const Opnd& B, GemmArgs args, bool split, cudaStream_t st);
+int num_sms();
+int pick_bn(int M, int N);   // tile width gemm_run will use for an M x N product
+
+}  // namespace ttt

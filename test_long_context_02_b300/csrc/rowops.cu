@@ -1,0 +1,432 @@
+// Row-wise kernels of the TTT-E2E inner-loop step: token embedding, RMSNorm
+// forward/backward, RoPE (angle table, rotation of q/k with the write of the
+// chunk's own k/v, and its transpose for the backward), the commit of the
+// chunk's keys/values into the k-slot window cache, the cross-entropy
+// combine/mean, and the rowsum(dO * O) term of the attention backward.
+//
+// All are HBM-bound: one warp per row, 16-byte vector loads/stores, fp32
+// arithmetic; operands for the tensor-core kernels are written as bf16
+// (plus the bf16 remainder in split mode).
+#include <cmath>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "rowops.h"
+
+namespace ttt {
+
+namespace {
+
+TTT_DEV float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// 8 consecutive fp32 values -> 8 bf16 (hi) [+ 8 bf16 remainders], one 16-B store each.
+TTT_DEV void store8(bf16* hi, bf16* lo, long off, const float (&v)[8]) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 t = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    h[i] = *reinterpret_cast<uint32_t*>(&t);
+    float2 f = __bfloat1622float2(t);
+    l[i] = pack_bf16(v[2 * i] - f.x, v[2 * i + 1] - f.y);
+  }
+  *reinterpret_cast<uint4*>(hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
+  if (lo) *reinterpret_cast<uint4*>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+TTT_DEV void load8(const float* p, float (&v)[8]) {
+  float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+TTT_DEV void load8_bf(const bf16* hi, const bf16* lo, long off, float (&v)[8]) {
+  uint4 h = *reinterpret_cast<const uint4*>(hi + off);
+  const __nv_bfloat162* hp = reinterpret_cast<const __nv_bfloat162*>(&h);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 f = __bfloat1622float2(hp[i]);
+    v[2 * i] = f.x;
+    v[2 * i + 1] = f.y;
+  }
+  if (lo) {
+    uint4 l = *reinterpret_cast<const uint4*>(lo + off);
+    const __nv_bfloat162* lp = reinterpret_cast<const __nv_bfloat162*>(&l);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float2 f = __bfloat1622float2(lp[i]);
+      v[2 * i] += f.x;
+      v[2 * i + 1] += f.y;
+    }
+  }
+}
+
+// x[t][:] = E[tok[t]][:]; bad ids are reported and read row 0.
+__global__ void embed_kernel(const int* __restrict__ tok, int n, const float* __restrict__ E, int V, int d,
+                             float* __restrict__ x, int* err) {
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (row >= n) return;
+  int id = tok[row];
+  if (id < 0 || id >= V) {
+    if (lane == 0 && err) atomicCAS(err, 0, (int)DERR_BAD_TOKEN);
+    id = 0;
+  }
+  const float4* src = reinterpret_cast<const float4*>(E + (long)id * d);
+  float4* dst = reinterpret_cast<float4*>(x + (long)row * d);
+  for (int i = lane; i < d / 4; i += 32) dst[i] = src[i];
+}
+
+// Next-token targets of the chunk: tgt[i] = tok[i+1] (i < n-1), tgt[n-1] = *next (-1: none).
+__global__ void targets_kernel(const int* __restrict__ tok, int n, const int* __restrict__ next, int V,
+                               int* __restrict__ tgt, int* err) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  int t = (i + 1 < n) ? tok[i + 1] : *next;
+  if (t >= V || t < -1) {
+    if (err) atomicCAS(err, 0, (int)DERR_BAD_TOKEN);
+    t = -1;
+  }
+  tgt[i] = t;
+}
+
+// y = x * g / sqrt(mean(x^2) + eps) -> bf16 (hi, lo); rstd saved when requested.
+__global__ void rmsnorm_kernel(const float* __restrict__ x, const float* __restrict__ g, float eps, int n, int d,
+                               bf16* __restrict__ yh, bf16* __restrict__ yl, float* __restrict__ rstd) {
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (row >= n) return;
+  const float* xr = x + (long)row * d;
+  float ss = 0.f;
+  for (int c = lane * 8; c < d; c += 256) {
+    float v[8];
+    load8(xr + c, v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ss += v[i] * v[i];
+  }
+  ss = warp_sum(ss);
+  const float r = 1.0f / sqrtf(ss / (float)d + eps);
+  if (rstd && lane == 0) rstd[row] = r;
+  for (int c = lane * 8; c < d; c += 256) {
+    float v[8], gg[8];
+    load8(xr + c, v);
+    load8(g + c, gg);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = v[i] * r * gg[i];
+    store8(yh, yl, (long)row * d + c, v);
+  }
+}
+
+// out = resid + [r g dy - x r^3/d * sum(dy g x)]  (gradient of RMSNorm w.r.t. its input, gain frozen)
+__global__ void rmsnorm_bwd_kernel(const float* __restrict__ dy, const float* __restrict__ x,
+                                   const float* __restrict__ g, const float* __restrict__ rstd,
+                                   const float* resid, int n, int d, float* out, bf16* __restrict__ oh,
+                                   bf16* __restrict__ ol) {
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (row >= n) return;
+  const long base = (long)row * d;
+  float s = 0.f;
+  for (int c = lane * 8; c < d; c += 256) {
+    float a[8], b[8], gg[8];
+    load8(dy + base + c, a);
+    load8(x + base + c, b);
+    load8(g + c, gg);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s += a[i] * gg[i] * b[i];
+  }
+  s = warp_sum(s);
+  const float r = rstd[row];
+  const float k = r * r * r * s / (float)d;
+  for (int c = lane * 8; c < d; c += 256) {
+    float a[8], b[8], gg[8], rr[8];
+    load8(dy + base + c, a);
+    load8(x + base + c, b);
+    load8(g + c, gg);
+    if (resid) {
+      load8(resid + base + c, rr);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) rr[i] = 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) rr[i] += r * gg[i] * a[i] - b[i] * k;
+    float4* o = reinterpret_cast<float4*>(out + base + c);
+    o[0] = make_float4(rr[0], rr[1], rr[2], rr[3]);
+    o[1] = make_float4(rr[4], rr[5], rr[6], rr[7]);
+    if (oh) store8(oh, ol, base + c, rr);
+  }
+}
+
+// cos/sin of pos * theta^(-2i/dh) for the chunk, angles formed and reduced in fp64.
+__global__ void rope_table_kernel(long pos0, int n, int half, const double* __restrict__ inv_freq,
+                                  float* __restrict__ cs, float* __restrict__ sn) {
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= n * half) return;
+  const int t = idx / half, i = idx % half;
+  double s, c;
+  sincos((double)(pos0 + t) * inv_freq[i], &s, &c);
+  cs[idx] = (float)c;
+  sn[idx] = (float)s;
+}
+
+// q' = rope(q), k' = rope(k), v from qkv[t][3d] (fp32); rotate-half pairs (i, i+dh/2).
+// One thread per (token, head, 4 pairs).
+__global__ void rope_qkv_kernel(const float* __restrict__ qkv, const float* __restrict__ cs,
+                                const float* __restrict__ sn, int n, int H, int dh, bf16* qh, bf16* ql, bf16* kh,
+                                bf16* kl, bf16* vh, bf16* vl) {
+  const int half = dh / 2, groups = half / 4;
+  const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (long)n * H * groups) return;
+  const int gi = (int)(idx % groups);
+  const int h = (int)((idx / groups) % H);
+  const int t = (int)(idx / ((long)groups * H));
+  const int d = H * dh, i0 = gi * 4;
+  const float* row = qkv + (long)t * 3 * d;
+  const float4 c4 = *reinterpret_cast<const float4*>(cs + (long)t * half + i0);
+  const float4 s4 = *reinterpret_cast<const float4*>(sn + (long)t * half + i0);
+  const float c[4] = {c4.x, c4.y, c4.z, c4.w}, s[4] = {s4.x, s4.y, s4.z, s4.w};
+  const long o1 = (long)t * d + h * dh + i0, o2 = o1 + half;
+#pragma unroll
+  for (int part = 0; part < 2; ++part) {  // 0: q, 1: k
+    const float* src = row + part * d + h * dh + i0;
+    const float4 a4 = *reinterpret_cast<const float4*>(src);
+    const float4 b4 = *reinterpret_cast<const float4*>(src + half);
+    const float a[4] = {a4.x, a4.y, a4.z, a4.w}, b[4] = {b4.x, b4.y, b4.z, b4.w};
+    bf16* oh = part ? kh : qh;
+    bf16* ol = part ? kl : ql;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float2 r;
+      r.x = a[j] * c[j] - b[j] * s[j];
+      r.y = b[j] * c[j] + a[j] * s[j];
+      __nv_bfloat16 x1h, x1l, x2h, x2l;
+      split_bf16(r.x, x1h, x1l);
+      split_bf16(r.y, x2h, x2l);
+      oh[o1 + j] = x1h;
+      oh[o2 + j] = x2h;
+      if (ol) {
+        ol[o1 + j] = x1l;
+        ol[o2 + j] = x2l;
+      }
+    }
+  }
+  const float* vs = row + 2 * d + h * dh + i0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    __nv_bfloat16 h1, l1, h2, l2;
+    split_bf16(vs[j], h1, l1);
+    split_bf16(vs[j + half], h2, l2);
+    vh[o1 + j] = h1;
+    vh[o2 + j] = h2;
+    if (vl) {
+      vl[o1 + j] = l1;
+      vl[o2 + j] = l2;
+    }
+  }
+}
+
+// Backward of the rotation (its transpose) for dq, dk; dv passes through.
+// Writes the concatenated [dq | dk | dv] rows (bf16 hi/lo) for the QKV dX product.
+__global__ void rope_bwd_kernel(const float* __restrict__ dq, const float* __restrict__ dk,
+                                const float* __restrict__ dv, const float* __restrict__ cs,
+                                const float* __restrict__ sn, int n, int H, int dh, bf16* oh, bf16* ol) {
+  const int half = dh / 2;
+  const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (long)n * H * half) return;
+  const int i = (int)(idx % half);
+  const int h = (int)((idx / half) % H);
+  const int t = (int)(idx / ((long)half * H));
+  const int d = H * dh;
+  const float c = cs[(long)t * half + i], s = sn[(long)t * half + i];
+  const long src1 = (long)t * d + h * dh + i, src2 = src1 + half;
+  const long dst = (long)t * 3 * d + h * dh + i;
+  const float q1 = dq[src1], q2 = dq[src2], k1 = dk[src1], k2 = dk[src2];
+  {
+    __nv_bfloat16 a, b;
+    split_bf16(q1 * c + q2 * s, a, b); oh[dst] = a; if (ol) ol[dst] = b;
+    split_bf16(q2 * c - q1 * s, a, b); oh[dst + half] = a; if (ol) ol[dst + half] = b;
+    split_bf16(k1 * c + k2 * s, a, b); oh[dst + d] = a; if (ol) ol[dst + d] = b;
+    split_bf16(k2 * c - k1 * s, a, b); oh[dst + d + half] = a; if (ol) ol[dst + d + half] = b;
+    split_bf16(dv[src1], a, b); oh[dst + 2 * d] = a; if (ol) ol[dst + 2 * d] = b;
+    split_bf16(dv[src2], a, b); oh[dst + 2 * d + half] = a; if (ol) ol[dst + 2 * d + half] = b;
+  }
+}
+
+// ring[(pos0 + t) mod k][:] = own[t][:] for the keys and values of every layer.
+// grid = (tokens, layers)
+__global__ void commit_kernel(const bf16* __restrict__ own, bf16* __restrict__ ring, long own_layer_stride,
+                              long ring_layer_stride, long pos0, int n, int window, int d) {
+  const int t = blockIdx.x;
+  const int l = blockIdx.y;
+  if (t >= n) return;
+  const long slot = (pos0 + t) % window;
+  const uint4* src = reinterpret_cast<const uint4*>(own + l * own_layer_stride + (long)t * d);
+  uint4* dst = reinterpret_cast<uint4*>(ring + l * ring_layer_stride + slot * d);
+  for (int i = threadIdx.x; i < d / 8; i += blockDim.x) dst[i] = src[i];
+}
+
+// lse[r] = log sum_tiles s_i exp(m_i); loss_row[r] = lse - z_target (0 when no target).
+__global__ void ce_combine_kernel(const float2* __restrict__ part, const float* __restrict__ zt,
+                                  const int* __restrict__ tgt, int n, int ntiles, float* __restrict__ lse,
+                                  float* __restrict__ loss_row) {
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= n) return;
+  float m = -INFINITY;
+  for (int i = 0; i < ntiles; ++i) m = fmaxf(m, part[(long)i * n + r].x);
+  float s = 0.f;
+  for (int i = 0; i < ntiles; ++i) {
+    const float2 p = part[(long)i * n + r];
+    s += p.y * expf(p.x - m);
+  }
+  const float l = m + logf(s);
+  lse[r] = l;
+  loss_row[r] = (tgt[r] >= 0) ? (l - zt[r]) : 0.f;
+}
+
+// Mean over the rows with a target, fixed reduction order (bit-reproducible).
+__global__ void loss_mean_kernel(const float* __restrict__ loss_row, const int* __restrict__ tgt, int n,
+                                 float* __restrict__ out, float* __restrict__ inv_count) {
+  __shared__ float ssum[32];
+  __shared__ int scnt[32];
+  float s = 0.f;
+  int c = 0;
+  for (int i = threadIdx.x; i < n; i += blockDim.x)
+    if (tgt[i] >= 0) {
+      s += loss_row[i];
+      ++c;
+    }
+  s = warp_sum(s);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+  if ((threadIdx.x & 31) == 0) {
+    ssum[threadIdx.x >> 5] = s;
+    scnt[threadIdx.x >> 5] = c;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float ts = 0.f;
+    int tc = 0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+      ts += ssum[w];
+      tc += scnt[w];
+    }
+    *out = tc > 0 ? ts / (float)tc : 0.f;
+    if (inv_count) *inv_count = tc > 0 ? 1.0f / (float)tc : 0.f;
+  }
+}
+
+// D[h][t] = sum_i dO[t][h dh + i] * O[t][h dh + i]  (one warp per (t, h))
+__global__ void attn_rowdot_kernel(const bf16* __restrict__ doh, const bf16* __restrict__ dol,
+                                   const bf16* __restrict__ oh, const bf16* __restrict__ ol, int n, int H,
+                                   int dh, float* __restrict__ D) {
+  const int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (w >= n * H) return;
+  const int t = w / H, h = w % H;
+  const long base = (long)t * H * dh + h * dh;
+  float s = 0.f;
+  for (int c = lane * 8; c < dh; c += 256) {
+    float a[8], b[8];
+    load8_bf(doh, dol, base + c, a);
+    load8_bf(oh, ol, base + c, b);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s += a[i] * b[i];
+  }
+  s = warp_sum(s);
+  if (lane == 0) D[(long)h * n + t] = s;
+}
+
+// dst[r][c] = split(src[r][c]) for r < rows, c < cols (weight upload / layout change).
+__global__ void convert_kernel(const float* __restrict__ src, long rows, int cols, long src_ld, bf16* dh, bf16* dl,
+                               long dst_ld) {
+  const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= rows * cols) return;
+  const long r = idx / cols;
+  const int c = (int)(idx % cols);
+  __nv_bfloat16 h, l;
+  split_bf16(src[r * src_ld + c], h, l);
+  dh[r * dst_ld + c] = h;
+  if (dl) dl[r * dst_ld + c] = l;
+}
+
+constexpr int kRowWarps = 8;
+inline int row_grid(int n) { return (n + kRowWarps - 1) / kRowWarps; }
+
+}  // namespace
+
+int rows_embed(const int* tok, int n, const float* E, int V, int d, float* x, int* err, cudaStream_t st) {
+  embed_kernel<<<row_grid(n), kRowWarps * 32, 0, st>>>(tok, n, E, V, d, x, err);
+  return (int)cudaGetLastError();
+}
+
+int rows_targets(const int* tok, int n, const int* next, int V, int* tgt, int* err, cudaStream_t st) {
+  targets_kernel<<<(n + 255) / 256, 256, 0, st>>>(tok, n, next, V, tgt, err);
+  return (int)cudaGetLastError();
+}
+
+int rows_rmsnorm(const float* x, const float* g, float eps, int n, int d, bf16* yh, bf16* yl, float* rstd,
+                 cudaStream_t st) {
+  rmsnorm_kernel<<<row_grid(n), kRowWarps * 32, 0, st>>>(x, g, eps, n, d, yh, yl, rstd);
+  return (int)cudaGetLastError();
+}
+
+int rows_rmsnorm_bwd(const float* dy, const float* x, const float* g, const float* rstd, const float* resid, int n,
+                     int d, float* out, bf16* oh, bf16* ol, cudaStream_t st) {
+  rmsnorm_bwd_kernel<<<row_grid(n), kRowWarps * 32, 0, st>>>(dy, x, g, rstd, resid, n, d, out, oh, ol);
+  return (int)cudaGetLastError();
+}
+
+int rows_rope_table(long pos0, int n, int dh, const double* inv_freq, float* cs, float* sn, cudaStream_t st) {
+  const int half = dh / 2, tot = n * half;
+  rope_table_kernel<<<(tot + 255) / 256, 256, 0, st>>>(pos0, n, half, inv_freq, cs, sn);
+  return (int)cudaGetLastError();
+}
+
+int rows_rope_qkv(const float* qkv, const float* cs, const float* sn, int n, int H, int dh, bf16* qh, bf16* ql,
+                  bf16* kh, bf16* kl, bf16* vh, bf16* vl, cudaStream_t st) {
+  const long tot = (long)n * H * (dh / 8);
+  rope_qkv_kernel<<<(unsigned)((tot + 255) / 256), 256, 0, st>>>(qkv, cs, sn, n, H, dh, qh, ql, kh, kl, vh, vl);
+  return (int)cudaGetLastError();
+}
+
+int rows_rope_bwd(const float* dq, const float* dk, const float* dv, const float* cs, const float* sn, int n, int H,
+                  int dh, bf16* oh, bf16* ol, cudaStream_t st) {
+  const long tot = (long)n * H * (dh / 2);
+  rope_bwd_kernel<<<(unsigned)((tot + 255) / 256), 256, 0, st>>>(dq, dk, dv, cs, sn, n, H, dh, oh, ol);
+  return (int)cudaGetLastError();
+}
+
+int rows_commit(const bf16* own, bf16* ring, long own_layer_stride, long ring_layer_stride, int n_layers, long pos0,
+                int n, int window, int d, cudaStream_t st) {
+  if (n <= 0 || n_layers <= 0) return 0;
+  dim3 grid(n, n_layers);
+  commit_kernel<<<grid, 128, 0, st>>>(own, ring, own_layer_stride, ring_layer_stride, pos0, n, window, d);
+  return (int)cudaGetLastError();
+}
+
+int rows_ce_combine(const float2* part, const float* zt, const int* tgt, int n, int ntiles, float* lse,
+                    float* loss_row, cudaStream_t st) {
+  ce_combine_kernel<<<(n + 127) / 128, 128, 0, st>>>(part, zt, tgt, n, ntiles, lse, loss_row);
+  return (int)cudaGetLastError();
+}
+
+int rows_loss_mean(const float* loss_row, const int* tgt, int n, float* out, float* inv_count, cudaStream_t st) {
+  loss_mean_kernel<<<1, 1024, 0, st>>>(loss_row, tgt, n, out, inv_count);
+  return (int)cudaGetLastError();
+}
+
+int rows_convert(const float* src, long rows, int cols, long src_ld, bf16* dh, bf16* dl, long dst_ld,
+                 cudaStream_t st) {
+  const long tot = rows * cols;
+  if (tot <= 0) return 0;
+  convert_kernel<<<(unsigned)((tot + 255) / 256), 256, 0, st>>>(src, rows, cols, src_ld, dh, dl, dst_ld);
+  return (int)cudaGetLastError();
+}
+
+int rows_attn_rowdot(const bf16* doh, const bf16* dol, const bf16* oh, const bf16* ol, int n, int H, int dh, float* D,
+                     cudaStream_t st) {
+  const int warps = n * H;
+  attn_rowdot_kernel<<<(warps + kRowWarps - 1) / kRowWarps, kRowWarps * 32, 0, st>>>(doh, dol, oh, ol, n, H, dh, D);
+  return (int)cudaGetLastError();
+}
+
+}  // namespace ttt

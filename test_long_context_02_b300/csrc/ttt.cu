@@ -1,0 +1,623 @@
+// libttt host orchestrator: the C ABI of include/ttt.h.
+//
+// One context = one model (frozen weights in bf16, plus the bf16 remainders in
+// the fp32-compute mode) and n_seqs independent sequences, each with its own
+// k-slot key/value window cache per layer and its own fp32 fast weights
+// (W_up, W_down of the last S blocks) with bf16 shadows used as GEMM operands.
+//
+// One inner-loop step of one sequence (pages: "把 Transformer 做成“终身学习者”：
+// TTT-E2E 如何让大模型边用边学？", §4.2 and §4.4; "TTT-E2E技术：突破大语言模型上下文限制的新范式",
+// §2.1), all on the context stream:
+//   forward  : embed; per block RMSNorm, QKV product, RoPE (+ own K/V), windowed
+//              attention, O product + residual, RMSNorm, up product + GELU,
+//              down product + residual; final RMSNorm; LM head fused with the
+//              vocab-tiled cross-entropy statistics; mean loss.
+//   backward : logit gradient (LM head recomputed) and its product with W_lm^T;
+//              final RMSNorm backward; for the trainable blocks, last first:
+//              dU = dY W_down^T (x GELU'), dW_down = U^T dY with the SGD step in
+//              its epilogue, dXn = dA W_up^T, dW_up = Xn^T dA with the SGD step,
+//              then (except for the first trainable block) RMSNorm backward,
+//              dO = dH Wo^T, attention backward, RoPE backward, dXn = dQKV Wqkv^T,
+//              RMSNorm backward.  Every dX product reads the weights before the
+//              step (it runs first on the stream); all gradients of the step are
+//              taken at the chunk's starting weights.
+//   commit   : the chunk's keys/values of every layer go into the window cache.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "attn.h"
+#include "kernels.h"
+#include "ptx.cuh"
+#include "rowops.h"
+#include "tmap.h"
+#include "ttt.h"
+
+using namespace ttt;
+
+namespace {
+
+struct Pair {  // bf16 operand (hi) and remainder (lo, split mode only)
+  bf16* hi = nullptr;
+  bf16* lo = nullptr;
+  Pair at(long off) const { return Pair{hi + off, lo ? lo + off : nullptr}; }
+};
+
+struct Seq {
+  long pos = 0;
+  Pair ring_k, ring_v;          // [L][k][d]
+  float* up32 = nullptr;        // [S][d][f]
+  float* down32 = nullptr;      // [S][f][d]
+  Pair up16, down16;            // shadows
+};
+
+}  // namespace
+
+struct ttt_ctx {
+  ttt_config cfg{};
+  cudaStream_t st = nullptr;
+  bool split = false, loaded = false;
+  std::string err;
+  int L = 0, S = 0, d = 0, H = 0, dh = 0, f = 0, V = 0, k = 0, b = 0, B = 0;
+  std::vector<void*> allocs;
+  // frozen weights
+  float* E = nullptr;        // [V][d]
+  float* gains = nullptr;    // [2L+1][d]: g_attn(l), g_mlp(l), g_final
+  Pair Wqkv, Wo, Wup, Wdown, Wlm;  // [L][d][3d], [L][d][d], [L-S][d][f], [L-S][f][d], [d][V]
+  std::vector<Seq> seqs;
+  // per-step device scratch
+  int *tok = nullptr, *tgt = nullptr, *next = nullptr, *minus1 = nullptr, *derr = nullptr;
+  float* loss_dev = nullptr;
+  double* inv_freq = nullptr;
+  float *cs = nullptr, *sn = nullptr;
+  float *x = nullptr, *qkv = nullptr, *a = nullptr;
+  Pair xn, q, o, u;
+  Pair kown, vown;           // [L][b][d]
+  float *sx = nullptr, *sh = nullptr, *srs_a = nullptr, *srs_m = nullptr, *slse = nullptr, *sa = nullptr;
+  Pair sq, so, sxm, su;
+  Pair xf, dz;
+  float *rs_f = nullptr, *zt = nullptr, *lse_row = nullptr, *loss_row = nullptr, *inv_nvalid = nullptr;
+  float2* part = nullptr;
+  float *dy = nullptr, *dxn = nullptr, *dh32 = nullptr, *D = nullptr, *dq = nullptr, *dk = nullptr, *dv = nullptr;
+  Pair dy16, da, dh16, do16, dqkv;
+};
+
+namespace {
+
+int fail(ttt_ctx* c, int code, const std::string& msg) {
+  if (c) c->err = msg;
+  return code;
+}
+
+#define CK(expr)                                                                                  \
+  do {                                                                                            \
+    int _r = (int)(expr);                                                                         \
+    if (_r != 0)                                                                                  \
+      return fail(c, TTT_ERR_CUDA, std::string(#expr) + ": " + cudaGetErrorString((cudaError_t)_r)); \
+  } while (0)
+
+template <typename T>
+T* dalloc(ttt_ctx* c, size_t count, bool& ok) {
+  void* p = nullptr;
+  if (!ok) return nullptr;
+  if (cudaMalloc(&p, count * sizeof(T) + 256) != cudaSuccess) {
+    ok = false;
+    cudaGetLastError();
+    return nullptr;
+  }
+  cudaMemset(p, 0, count * sizeof(T) + 256);
+  c->allocs.push_back(p);
+  return static_cast<T*>(p);
+}
+
+Pair palloc(ttt_ctx* c, size_t count, bool& ok) {
+  Pair p;
+  p.hi = dalloc<bf16>(c, count, ok);
+  if (c->split) p.lo = dalloc<bf16>(c, count, ok);
+  return p;
+}
+
+Opnd opnd(const Pair& p, long ld, int mn) {
+  Opnd o;
+  o.hi = p.hi;
+  o.lo = p.lo;
+  o.ld = ld;
+  o.mn = mn;
+  return o;
+}
+
+bool attn_maps(AttnMaps* m, const Pair& q, const Pair& kr, const Pair& vr, const Pair& ko, const Pair& vo, int n,
+               int d, int window) {
+  auto mk = [&](CUtensorMap* t, const bf16* p, int rows) { return make_map(t, p, (uint64_t)d, (uint64_t)rows, d, 128); };
+  bool ok = mk(&m->q, q.hi, n) && mk(&m->kr, kr.hi, window) && mk(&m->vr, vr.hi, window) && mk(&m->ko, ko.hi, n) &&
+            mk(&m->vo, vo.hi, n);
+  if (!ok) return false;
+  if (q.lo) {
+    ok = mk(&m->ql, q.lo, n) && mk(&m->krl, kr.lo, window) && mk(&m->vrl, vr.lo, window) && mk(&m->kol, ko.lo, n) &&
+         mk(&m->vol, vo.lo, n);
+  } else {
+    m->ql = m->q;
+    m->krl = m->kr;
+    m->vrl = m->vr;
+    m->kol = m->ko;
+    m->vol = m->vo;
+  }
+  return ok;
+}
+
+// One inner-loop step of sequence s: tokens tok[n] / next target next[1] on the device.
+int step(ttt_ctx* c, int s, const int* tok, int n, const int* next, float* loss_out) {
+  Seq& sq_ = c->seqs[s];
+  cudaStream_t st = c->st;
+  const int L = c->L, S = c->S, d = c->d, H = c->H, dh = c->dh, f = c->f, V = c->V, k = c->k, b = c->b;
+  const long pos0 = sq_.pos;
+  const bool sp = c->split;
+  const int P0 = L - S;  // first trainable block
+  const float eta = c->cfg.eta;
+
+  CK(rows_targets(tok, n, next, V, c->tgt, c->derr, st));
+  CK(rows_embed(tok, n, c->E, V, d, c->x, c->derr, st));
+  CK(rows_rope_table(pos0, n, dh, c->inv_freq, c->cs, c->sn, st));
+
+  auto in_ptr = [&](int l) -> float* { return l >= P0 ? c->sx + (long)(l - P0) * b * d : c->x; };
+
+  AttnArgs aa;
+  aa.n = n;
+  aa.H = H;
+  aa.dh = dh;
+  aa.window = k;
+  aa.pos0 = pos0;
+  aa.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)dh));
+  aa.ldo = d;
+  aa.err = c->derr;
+
+  // ------------------------------------------------------------------ forward
+  if (P0 == 0) CK(cudaMemcpyAsync(c->sx, c->x, (size_t)n * d * 4, cudaMemcpyDeviceToDevice, st));
+  for (int l = 0; l < L; ++l) {
+    const bool suf = l >= P0;
+    const int si = l - P0;
+    float* xin = in_ptr(l);
+    float* xout = (l + 1 < L) ? in_ptr(l + 1) : c->x;
+    float* hbuf = suf ? c->sh + (long)si * b * d : xin;
+    Pair xn_a = c->xn;
+    Pair qb = suf ? c->sq.at((long)si * b * d) : c->q;
+    Pair ob = suf ? c->so.at((long)si * b * d) : c->o;
+    Pair xn_m = suf ? c->sxm.at((long)si * b * d) : c->xn;
+    float* abuf = suf ? c->sa + (long)si * b * f : c->a;
+    Pair ub = suf ? c->su.at((long)si * b * f) : c->u;
+    Pair ko = c->kown.at((long)l * b * d), vo = c->vown.at((long)l * b * d);
+    Pair kr = sq_.ring_k.at((long)l * k * d), vr = sq_.ring_v.at((long)l * k * d);
+
+    CK(rows_rmsnorm(xin, c->gains + (long)(2 * l) * d, c->cfg.rms_eps, n, d, xn_a.hi, xn_a.lo,
+                    suf ? c->srs_a + (long)si * b : nullptr, st));
+    {
+      GemmArgs g;
+      g.M = n; g.N = 3 * d; g.K = d;
+      g.out32 = c->qkv; g.ldo32 = 3 * d; g.err = c->derr;
+      CK(gemm_run(EPI_F32, opnd(xn_a, d, 0), opnd(c->Wqkv.at((long)l * d * 3 * d), 3 * d, 1), g, sp, st));
+    }
+    CK(rows_rope_qkv(c->qkv, c->cs, c->sn, n, H, dh, qb.hi, qb.lo, ko.hi, ko.lo, vo.hi, vo.lo, st));
+    {
+      AttnMaps m;
+      if (!attn_maps(&m, qb, kr, vr, ko, vo, n, d, k)) return fail(c, TTT_ERR_CUDA, "attention tensor maps");
+      AttnArgs a2 = aa;
+      a2.o_hi = ob.hi;
+      a2.o_lo = ob.lo;
+      a2.lse = suf ? c->slse + (long)si * H * b : nullptr;
+      CK(attn_fwd_run(m, a2, sp, st));
+    }
+    {
+      GemmArgs g;
+      g.M = n; g.N = d; g.K = d;
+      g.out32 = hbuf; g.ldo32 = d; g.resid = xin; g.ldr = d; g.err = c->derr;
+      CK(gemm_run(EPI_RESID, opnd(ob, d, 0), opnd(c->Wo.at((long)l * d * d), d, 1), g, sp, st));
+    }
+    CK(rows_rmsnorm(hbuf, c->gains + (long)(2 * l + 1) * d, c->cfg.rms_eps, n, d, xn_m.hi, xn_m.lo,
+                    suf ? c->srs_m + (long)si * b : nullptr, st));
+    {
+      GemmArgs g;
+      g.M = n; g.N = f; g.K = d;
+      g.out32 = abuf; g.ldo32 = f; g.oh = ub.hi; g.ol = ub.lo; g.ldo = f; g.err = c->derr;
+      Pair w = suf ? sq_.up16.at((long)si * d * f) : c->Wup.at((long)l * d * f);
+      CK(gemm_run(EPI_GELU, opnd(xn_m, d, 0), opnd(w, f, 1), g, sp, st));
+    }
+    {
+      GemmArgs g;
+      g.M = n; g.N = d; g.K = f;
+      g.out32 = xout; g.ldo32 = d; g.resid = hbuf; g.ldr = d; g.err = c->derr;
+      Pair w = suf ? sq_.down16.at((long)si * f * d) : c->Wdown.at((long)l * f * d);
+      CK(gemm_run(EPI_RESID, opnd(ub, f, 0), opnd(w, d, 1), g, sp, st));
+    }
+  }
+  // final norm + LM head + cross-entropy statistics
+  CK(rows_rmsnorm(c->x, c->gains + (long)(2 * L) * d, c->cfg.rms_eps, n, d, c->xf.hi, c->xf.lo, c->rs_f, st));
+  const int bn = pick_bn(n, V);
+  const int ntiles = (V + bn - 1) / bn;
+  {
+    GemmArgs g;
+    g.M = n; g.N = V; g.K = d;
+    g.tgt = c->tgt; g.part = c->part; g.zt = c->zt; g.err = c->derr;
+    CK(gemm_run(EPI_CE_FWD, opnd(c->xf, d, 0), opnd(c->Wlm, V, 1), g, sp, st));
+  }
+  CK(rows_ce_combine(c->part, c->zt, c->tgt, n, ntiles, c->lse_row, c->loss_row, st));
+  CK(rows_loss_mean(c->loss_row, c->tgt, n, loss_out, c->inv_nvalid, st));
+
+  // ----------------------------------------------------------------- backward
+  {  // dZ = (softmax(Z) - onehot(target)) / n_valid, logits recomputed tile by tile
+    GemmArgs g;
+    g.M = n; g.N = V; g.K = d;
+    g.tgt = c->tgt; g.lse = c->lse_row; g.scale_dev = c->inv_nvalid;
+    g.oh = c->dz.hi; g.ol = c->dz.lo; g.ldo = V; g.err = c->derr;
+    CK(gemm_run(EPI_CE_BWD, opnd(c->xf, d, 0), opnd(c->Wlm, V, 1), g, sp, st));
+  }
+  {
+    GemmArgs g;
+    g.M = n; g.N = d; g.K = V;
+    g.out32 = c->dxn; g.ldo32 = d; g.err = c->derr;
+    CK(gemm_run(EPI_F32, opnd(c->dz, V, 0), opnd(c->Wlm, V, 0), g, sp, st));
+  }
+  CK(rows_rmsnorm_bwd(c->dxn, c->x, c->gains + (long)(2 * L) * d, c->rs_f, nullptr, n, d, c->dy, c->dy16.hi,
+                      c->dy16.lo, st));
+  for (int si = S - 1; si >= 0; --si) {
+    const int l = P0 + si;
+    Pair up16 = sq_.up16.at((long)si * d * f), down16 = sq_.down16.at((long)si * f * d);
+    {  // dA = (dY W_down^T) * gelu'(a)
+      GemmArgs g;
+      g.M = n; g.N = f; g.K = d;
+      g.aux = c->sa + (long)si * b * f; g.ldaux = f;
+      g.oh = c->da.hi; g.ol = c->da.lo; g.ldo = f; g.err = c->derr;
+      CK(gemm_run(EPI_GELU_BWD, opnd(c->dy16, d, 0), opnd(down16, d, 0), g, sp, st));
+    }
+    {  // W_down -= eta U^T dY
+      GemmArgs g;
+      g.M = f; g.N = d; g.K = n;
+      g.w32 = sq_.down32 + (long)si * f * d; g.wh = down16.hi; g.wl = down16.lo; g.ldw = d; g.eta = eta;
+      g.err = c->derr;
+      CK(gemm_run(EPI_SGD, opnd(c->su.at((long)si * b * f), f, 1), opnd(c->dy16, d, 1), g, sp, st));
+    }
+    if (si > 0) {  // dXn_m = dA W_up^T  (before W_up changes)
+      GemmArgs g;
+      g.M = n; g.N = d; g.K = f;
+      g.out32 = c->dxn; g.ldo32 = d; g.err = c->derr;
+      CK(gemm_run(EPI_F32, opnd(c->da, f, 0), opnd(up16, f, 0), g, sp, st));
+    }
+    {  // W_up -= eta Xn_m^T dA
+      GemmArgs g;
+      g.M = d; g.N = f; g.K = n;
+      g.w32 = sq_.up32 + (long)si * d * f; g.wh = up16.hi; g.wl = up16.lo; g.ldw = f; g.eta = eta;
+      g.err = c->derr;
+      CK(gemm_run(EPI_SGD, opnd(c->sxm.at((long)si * b * d), d, 1), opnd(c->da, f, 1), g, sp, st));
+    }
+    if (si == 0) break;  // the first trainable block's attention needs no gradient
+    // dH = dY + RMSNorm_m^T(dXn_m)
+    CK(rows_rmsnorm_bwd(c->dxn, c->sh + (long)si * b * d, c->gains + (long)(2 * l + 1) * d, c->srs_m + (long)si * b,
+                        c->dy, n, d, c->dh32, c->dh16.hi, c->dh16.lo, st));
+    {  // dO = dH Wo^T
+      GemmArgs g;
+      g.M = n; g.N = d; g.K = d;
+      g.oh = c->do16.hi; g.ol = c->do16.lo; g.ldo = d; g.err = c->derr;
+      CK(gemm_run(EPI_OPND, opnd(c->dh16, d, 0), opnd(c->Wo.at((long)l * d * d), d, 0), g, sp, st));
+    }
+    Pair qb = c->sq.at((long)si * b * d), ob = c->so.at((long)si * b * d);
+    CK(rows_attn_rowdot(c->do16.hi, c->do16.lo, ob.hi, ob.lo, n, H, dh, c->D, st));
+    {
+      AttnBwdMaps m;
+      Pair ko = c->kown.at((long)l * b * d), vo = c->vown.at((long)l * b * d);
+      Pair kr = sq_.ring_k.at((long)l * k * d), vr = sq_.ring_v.at((long)l * k * d);
+      if (!attn_maps(&m.f, qb, kr, vr, ko, vo, n, d, k) ||
+          !make_map(&m.dO, c->do16.hi, (uint64_t)d, (uint64_t)n, d, 128))
+        return fail(c, TTT_ERR_CUDA, "attention backward tensor maps");
+      if (sp) {
+        if (!make_map(&m.dOl, c->do16.lo, (uint64_t)d, (uint64_t)n, d, 128))
+          return fail(c, TTT_ERR_CUDA, "attention backward tensor maps");
+      } else {
+        m.dOl = m.dO;
+      }
+      AttnBwdArgs ba;
+      ba.g = aa;
+      ba.lse = c->slse + (long)si * H * b;
+      ba.D = c->D;
+      ba.dq = c->dq;
+      ba.dk = c->dk;
+      ba.dv = c->dv;
+      ba.ldg = d;
+      ba.scale = (float)(1.0 / std::sqrt((double)dh));
+      CK(attn_bwd_run(m, ba, sp, st));
+    }
+    CK(rows_rope_bwd(c->dq, c->dk, c->dv, c->cs, c->sn, n, H, dh, c->dqkv.hi, c->dqkv.lo, st));
+    {  // dXn_a = dQKV Wqkv^T
+      GemmArgs g;
+      g.M = n; g.N = d; g.K = 3 * d;
+      g.out32 = c->dxn; g.ldo32 = d; g.err = c->derr;
+      CK(gemm_run(EPI_F32, opnd(c->dqkv, 3 * d, 0), opnd(c->Wqkv.at((long)l * d * 3 * d), 3 * d, 0), g, sp, st));
+    }
+    // dY_{l-1} = dH + RMSNorm_a^T(dXn_a)
+    CK(rows_rmsnorm_bwd(c->dxn, c->sx + (long)si * b * d, c->gains + (long)(2 * l) * d, c->srs_a + (long)si * b,
+                        c->dh32, n, d, c->dy, c->dy16.hi, c->dy16.lo, st));
+  }
+  // ------------------------------------------------------------------- commit
+  CK(rows_commit(c->kown.hi, sq_.ring_k.hi, (long)b * d, (long)k * d, L, pos0, n, k, d, st));
+  CK(rows_commit(c->vown.hi, sq_.ring_v.hi, (long)b * d, (long)k * d, L, pos0, n, k, d, st));
+  if (sp) {
+    CK(rows_commit(c->kown.lo, sq_.ring_k.lo, (long)b * d, (long)k * d, L, pos0, n, k, d, st));
+    CK(rows_commit(c->vown.lo, sq_.ring_v.lo, (long)b * d, (long)k * d, L, pos0, n, k, d, st));
+  }
+  sq_.pos = pos0 + n;
+  return TTT_OK;
+}
+
+}  // namespace
+
+// ============================================================================ C ABI
+extern "C" int ttt_create(const ttt_config* cfg, void* cuda_stream, ttt_ctx** out) {
+  if (!cfg || !out) return TTT_ERR_ARG;
+  *out = nullptr;
+  const ttt_config& g = *cfg;
+  if (g.n_layers <= 0 || g.n_trainable <= 0 || g.n_trainable > g.n_layers || g.d_model <= 0 || g.n_heads <= 0 ||
+      g.d_ff <= 0 || g.vocab <= 0 || g.window <= 0 || g.chunk <= 0 || g.n_seqs <= 0 || g.chunk > g.window ||
+      g.d_model % g.n_heads != 0 || !(g.rope_theta > 0) || !(g.rms_eps >= 0) || (g.compute != 0 && g.compute != 1))
+    return TTT_ERR_ARG;
+  const int dh = g.d_model / g.n_heads;
+  const bool split = g.compute == 0;
+  if (dh % 16 || dh > 128 || (split && dh > 64) || g.d_model % 64 || g.d_ff % 64 || g.vocab % 8 || g.window % 128)
+    return TTT_ERR_UNSUPPORTED;
+  ttt_ctx* c = new ttt_ctx();
+  c->cfg = g;
+  c->st = (cudaStream_t)cuda_stream;
+  c->split = split;
+  c->L = g.n_layers; c->S = g.n_trainable; c->d = g.d_model; c->H = g.n_heads; c->dh = dh; c->f = g.d_ff;
+  c->V = g.vocab; c->k = g.window; c->b = g.chunk; c->B = g.n_seqs;
+  const long L = c->L, S = c->S, d = c->d, f = c->f, V = c->V, k = c->k, b = c->b, H = c->H;
+  bool ok = true;
+  c->E = dalloc<float>(c, V * d, ok);
+  c->gains = dalloc<float>(c, (2 * L + 1) * d, ok);
+  c->Wqkv = palloc(c, L * d * 3 * d, ok);
+  c->Wo = palloc(c, L * d * d, ok);
+  c->Wup = palloc(c, (L - S) * d * f, ok);
+  c->Wdown = palloc(c, (L - S) * f * d, ok);
+  c->Wlm = palloc(c, d * V, ok);
+  c->seqs.resize(g.n_seqs);
+  for (auto& s : c->seqs) {
+    s.ring_k = palloc(c, L * k * d, ok);
+    s.ring_v = palloc(c, L * k * d, ok);
+    s.up32 = dalloc<float>(c, S * d * f, ok);
+    s.down32 = dalloc<float>(c, S * f * d, ok);
+    s.up16 = palloc(c, S * d * f, ok);
+    s.down16 = palloc(c, S * f * d, ok);
+  }
+  c->tok = dalloc<int>(c, (size_t)g.n_seqs * b, ok);
+  c->tgt = dalloc<int>(c, b, ok);
+  c->next = dalloc<int>(c, g.n_seqs, ok);
+  c->minus1 = dalloc<int>(c, 1, ok);
+  c->derr = dalloc<int>(c, 1, ok);
+  c->loss_dev = dalloc<float>(c, g.n_seqs, ok);
+  c->inv_freq = dalloc<double>(c, dh / 2, ok);
+  c->cs = dalloc<float>(c, b * dh / 2, ok);
+  c->sn = dalloc<float>(c, b * dh / 2, ok);
+  c->x = dalloc<float>(c, b * d, ok);
+  c->qkv = dalloc<float>(c, b * 3 * d, ok);
+  c->a = dalloc<float>(c, b * f, ok);
+  c->xn = palloc(c, b * d, ok);
+  c->q = palloc(c, b * d, ok);
+  c->o = palloc(c, b * d, ok);
+  c->u = palloc(c, b * f, ok);
+  c->kown = palloc(c, L * b * d, ok);
+  c->vown = palloc(c, L * b * d, ok);
+  c->sx = dalloc<float>(c, S * b * d, ok);
+  c->sh = dalloc<float>(c, S * b * d, ok);
+  c->srs_a = dalloc<float>(c, S * b, ok);
+  c->srs_m = dalloc<float>(c, S * b, ok);
+  c->slse = dalloc<float>(c, S * H * b, ok);
+  c->sa = dalloc<float>(c, S * b * f, ok);
+  c->sq = palloc(c, S * b * d, ok);
+  c->so = palloc(c, S * b * d, ok);
+  c->sxm = palloc(c, S * b * d, ok);
+  c->su = palloc(c, S * b * f, ok);
+  c->xf = palloc(c, b * d, ok);
+  c->dz = palloc(c, b * V, ok);
+  c->rs_f = dalloc<float>(c, b, ok);
+  c->zt = dalloc<float>(c, b, ok);
+  c->lse_row = dalloc<float>(c, b, ok);
+  c->loss_row = dalloc<float>(c, b, ok);
+  c->inv_nvalid = dalloc<float>(c, 1, ok);
+  c->part = dalloc<float2>(c, ((V + 127) / 128) * b, ok);
+  c->dy = dalloc<float>(c, b * d, ok);
+  c->dxn = dalloc<float>(c, b * d, ok);
+  c->dh32 = dalloc<float>(c, b * d, ok);
+  c->D = dalloc<float>(c, H * b, ok);
+  c->dq = dalloc<float>(c, b * d, ok);
+  c->dk = dalloc<float>(c, b * d, ok);
+  c->dv = dalloc<float>(c, b * d, ok);
+  c->dy16 = palloc(c, b * d, ok);
+  c->da = palloc(c, b * f, ok);
+  c->dh16 = palloc(c, b * d, ok);
+  c->do16 = palloc(c, b * d, ok);
+  c->dqkv = palloc(c, b * 3 * d, ok);
+  if (!ok) {
+    ttt_destroy(c);
+    return TTT_ERR_OOM;
+  }
+  std::vector<double> invf(dh / 2);
+  for (int i = 0; i < dh / 2; ++i) invf[i] = std::pow(g.rope_theta, -2.0 * i / (double)dh);
+  int m1 = -1;
+  if (cudaMemcpy(c->inv_freq, invf.data(), invf.size() * sizeof(double), cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemcpy(c->minus1, &m1, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess) {
+    ttt_destroy(c);
+    return TTT_ERR_CUDA;
+  }
+  *out = c;
+  return TTT_OK;
+}
+
+extern "C" void ttt_destroy(ttt_ctx* c) {
+  if (!c) return;
+  if (c->st) cudaStreamSynchronize(c->st);
+  cudaDeviceSynchronize();
+  for (void* p : c->allocs) cudaFree(p);
+  delete c;
+}
+
+extern "C" const char* ttt_last_error(const ttt_ctx* c) { return c ? c->err.c_str() : "null context"; }
+
+extern "C" int64_t ttt_position(const ttt_ctx* c) { return (c && !c->seqs.empty()) ? c->seqs[0].pos : -1; }
+
+extern "C" int ttt_load_weights(ttt_ctx* c, const float* blob, size_t n_floats) {
+  if (!c || !blob) return TTT_ERR_ARG;
+  const long L = c->L, S = c->S, d = c->d, f = c->f, V = c->V;
+  const size_t need = (size_t)(V * d + L * (2 * d + 4 * d * d + 2 * d * f) + d + d * V);
+  if (n_floats != need) return fail(c, TTT_ERR_ARG, "blob size " + std::to_string(n_floats) + " != " + std::to_string(need));
+  c->loaded = false;
+  cudaStream_t st = c->st;
+  float* stage = nullptr;
+  if (cudaMalloc(&stage, need * sizeof(float)) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(c, TTT_ERR_OOM, "weight staging buffer");
+  }
+  auto body = [&]() -> int {
+    CK(cudaMemcpyAsync(stage, blob, need * sizeof(float), cudaMemcpyHostToDevice, st));
+    long off = 0;
+    CK(cudaMemcpyAsync(c->E, stage, (size_t)V * d * 4, cudaMemcpyDeviceToDevice, st));
+    off += V * d;
+    for (long l = 0; l < L; ++l) {
+      CK(cudaMemcpyAsync(c->gains + (2 * l) * d, stage + off, (size_t)d * 4, cudaMemcpyDeviceToDevice, st));
+      off += d;
+      for (int part = 0; part < 3; ++part) {  // Wq | Wk | Wv -> columns of Wqkv[l]
+        Pair dst = c->Wqkv.at(l * d * 3 * d + part * d);
+        CK(rows_convert(stage + off, d, (int)d, d, dst.hi, dst.lo, 3 * d, st));
+        off += d * d;
+      }
+      Pair wo = c->Wo.at(l * d * d);
+      CK(rows_convert(stage + off, d, (int)d, d, wo.hi, wo.lo, d, st));
+      off += d * d;
+      CK(cudaMemcpyAsync(c->gains + (2 * l + 1) * d, stage + off, (size_t)d * 4, cudaMemcpyDeviceToDevice, st));
+      off += d;
+      const float* up = stage + off;
+      const float* down = stage + off + d * f;
+      off += 2 * d * f;
+      if (l < L - S) {
+        Pair wu = c->Wup.at(l * d * f), wd = c->Wdown.at(l * f * d);
+        CK(rows_convert(up, d, (int)f, f, wu.hi, wu.lo, f, st));
+        CK(rows_convert(down, f, (int)d, d, wd.hi, wd.lo, d, st));
+      } else {
+        const long si = l - (L - S);
+        for (auto& s : c->seqs) {
+          CK(cudaMemcpyAsync(s.up32 + si * d * f, up, (size_t)d * f * 4, cudaMemcpyDeviceToDevice, st));
+          CK(cudaMemcpyAsync(s.down32 + si * f * d, down, (size_t)f * d * 4, cudaMemcpyDeviceToDevice, st));
+          Pair wu = s.up16.at(si * d * f), wd = s.down16.at(si * f * d);
+          CK(rows_convert(up, d, (int)f, f, wu.hi, wu.lo, f, st));
+          CK(rows_convert(down, f, (int)d, d, wd.hi, wd.lo, d, st));
+        }
+      }
+    }
+    CK(cudaMemcpyAsync(c->gains + (2 * L) * d, stage + off, (size_t)d * 4, cudaMemcpyDeviceToDevice, st));
+    off += d;
+    CK(rows_convert(stage + off, d, (int)V, V, c->Wlm.hi, c->Wlm.lo, V, st));
+    off += d * V;
+    for (auto& s : c->seqs) {
+      s.pos = 0;
+      const size_t rb = (size_t)L * c->k * d * sizeof(bf16);
+      CK(cudaMemsetAsync(s.ring_k.hi, 0, rb, st));
+      CK(cudaMemsetAsync(s.ring_v.hi, 0, rb, st));
+      if (c->split) {
+        CK(cudaMemsetAsync(s.ring_k.lo, 0, rb, st));
+        CK(cudaMemsetAsync(s.ring_v.lo, 0, rb, st));
+      }
+    }
+    CK(cudaMemsetAsync(c->derr, 0, sizeof(int), st));
+    CK(cudaStreamSynchronize(st));
+    return TTT_OK;
+  };
+  const int r = body();
+  cudaStreamSynchronize(st);
+  cudaFree(stage);
+  if (r == TTT_OK) {
+    c->loaded = true;
+    c->err.clear();
+  }
+  return r;
+}
+
+namespace {
+int check_device_error(ttt_ctx* c) {
+  int e = 0;
+  if (cudaMemcpy(&e, c->derr, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return fail(c, TTT_ERR_CUDA, "reading the device error word");
+  if (e != 0) {
+    c->loaded = false;
+    return fail(c, TTT_ERR_DEVICE, e == DERR_BAD_TOKEN ? "token id outside [0, vocab)"
+                                                        : "bounded wait expired in a kernel (code " + std::to_string(e) + ")");
+  }
+  return TTT_OK;
+}
+}  // namespace
+
+extern "C" int ttt_sync(ttt_ctx* c) {
+  if (!c) return TTT_ERR_ARG;
+  cudaError_t e = cudaStreamSynchronize(c->st);
+  if (e != cudaSuccess) return fail(c, TTT_ERR_CUDA, cudaGetErrorString(e));
+  return check_device_error(c);
+}
+
+extern "C" int ttt_prefill_chunk_dev(ttt_ctx* c, const int32_t* d_tokens, int32_t n, const int32_t* d_next,
+                                     float* d_loss) {
+  if (!c || !d_tokens || !d_next || !d_loss) return TTT_ERR_ARG;
+  if (!c->loaded) return fail(c, TTT_ERR_STATE, "weights not loaded");
+  if (n < 1 || n > c->b) return fail(c, TTT_ERR_ARG, "n outside 1..chunk");
+  for (int s = 0; s < c->B; ++s) {
+    const int r = step(c, s, d_tokens + (long)s * n, n, d_next + s, d_loss + s);
+    if (r != TTT_OK) return r;
+  }
+  return TTT_OK;
+}
+
+extern "C" int ttt_prefill_chunk(ttt_ctx* c, const int32_t* tokens, int32_t n, const int32_t* next_tokens,
+                                 float* chunk_loss) {
+  if (!c || !tokens || !next_tokens || !chunk_loss) return TTT_ERR_ARG;
+  if (!c->loaded) return fail(c, TTT_ERR_STATE, "weights not loaded");
+  if (n < 1 || n > c->b) return fail(c, TTT_ERR_ARG, "n outside 1..chunk");
+  for (long i = 0; i < (long)c->B * n; ++i)
+    if (tokens[i] < 0 || tokens[i] >= c->V) return fail(c, TTT_ERR_ARG, "token id outside [0, vocab)");
+  for (int s = 0; s < c->B; ++s)
+    if (next_tokens[s] < -1 || next_tokens[s] >= c->V) return fail(c, TTT_ERR_ARG, "next token outside [-1, vocab)");
+  if (cudaMemcpyAsync(c->tok, tokens, (size_t)c->B * n * sizeof(int), cudaMemcpyHostToDevice, c->st) != cudaSuccess ||
+      cudaMemcpyAsync(c->next, next_tokens, (size_t)c->B * sizeof(int), cudaMemcpyHostToDevice, c->st) != cudaSuccess)
+    return fail(c, TTT_ERR_CUDA, "token upload");
+  int r = ttt_prefill_chunk_dev(c, c->tok, n, c->next, c->loss_dev);
+  if (r != TTT_OK) return r;
+  if (cudaMemcpyAsync(chunk_loss, c->loss_dev, (size_t)c->B * sizeof(float), cudaMemcpyDeviceToHost, c->st) !=
+      cudaSuccess)
+    return fail(c, TTT_ERR_CUDA, "loss download");
+  return ttt_sync(c);
+}
+
+extern "C" int ttt_prefill_sequence_dev(ttt_ctx* c, const int32_t* d_tokens, int32_t T, float* d_losses) {
+  if (!c || !d_tokens || !d_losses || T < 1) return TTT_ERR_ARG;
+  if (!c->loaded) return fail(c, TTT_ERR_STATE, "weights not loaded");
+  const int b = c->b;
+  const int nc = (T + b - 1) / b;
+  for (int ci = 0; ci < nc; ++ci) {
+    const int s0 = ci * b, n = std::min(b, T - s0);
+    for (int s = 0; s < c->B; ++s) {
+      const int32_t* tk = d_tokens + (long)s * T + s0;
+      const int32_t* nx = (s0 + n < T) ? tk + n : c->minus1;
+      const int r = step(c, s, tk, n, nx, d_losses + (long)s * nc + ci);
+      if (r != TTT_OK) return r;
+    }
+  }
+  return TTT_OK;
+}
+
+extern "C" int ttt_get_fast_weights(ttt_ctx* c, int32_t seq, int32_t sl, float* w_up, float* w_down) {
+  if (!c || seq < 0 || seq >= c->B || sl < 0 || sl >= c->S) return TTT_ERR_ARG;
+  const long d = c->d, f = c->f;
+  cudaError_t e = cudaStreamSynchronize(c->st);
+  if (e == cudaSuccess && w_up)
+    e = cudaMemcpy(w_up, c->seqs[seq].up32 + sl * d * f, (size_t)d * f * 4, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && w_down)
+    e = cudaMemcpy(w_down, c->seqs[seq].down32 + sl * f * d, (size_t)f * d * 4, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail(c, TTT_ERR_CUDA, cudaGetErrorString(e));
+  return TTT_OK;
+}

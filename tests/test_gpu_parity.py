@@ -1,0 +1,127 @@
+"""The whole inner loop (libttt through its C ABI) against the float64 oracle.
+
+Same seeded tokens and fp32 weights on both sides; per-chunk losses and the
+final fast weights are compared with the tolerances of the method's statement:
+fp32 compute: loss 1e-4 relative, fast weights 1e-4 relative Frobenius;
+bf16 compute (fp32 fast weights): loss 2e-2 relative, fast weights 1e-2.
+The relative error of the update itself, |dW_gpu - dW_ref| / |dW_ref|, is
+printed as a stricter diagnostic (not gated).
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+import test_long_context_02_b300 as T  # noqa: E402
+from oracle import ttt_oracle as O  # noqa: E402
+from ttt_inputs import SHAPES, Shape, sequence_tokens, weight_blob, zipf_tokens  # noqa: E402
+
+TOL = {"fp32": (1e-4, 1e-4), "bf16": (2e-2, 1e-2)}
+
+# small shapes that still span several tiles, wrap the window cache and end in a ragged chunk
+SMALL = {
+    "dh64": Shape(8, 256, 4, 1024, 1000, 256, 128, 1e4, 1e-2, 1000),
+    "dh96": Shape(8, 384, 4, 1536, 2048, 256, 256, 1e6, 1e-2, 900),
+    "dh128": Shape(8, 512, 4, 2048, 1024, 512, 256, 1e7, 1e-2, 1100),
+    "fp32_dh64": Shape(8, 256, 4, 1024, 512, 128, 128, 1e4, 1e-2, 700, compute="fp32"),
+}
+
+
+def rel(a, b):
+    return float(np.linalg.norm(np.asarray(a, np.float64) - b) / max(np.linalg.norm(b), 1e-30))
+
+
+def run_gpu(shape, tokens, blob):
+    m = T.TTT.from_shape(shape)
+    m.load_weights(blob)
+    b, Tn = shape.chunk, len(tokens)
+    losses = []
+    for s in range(0, Tn, b):
+        n = min(b, Tn - s)
+        nxt = int(tokens[s + n]) if s + n < Tn else -1
+        losses.append(float(m.prefill_chunk(tokens[s:s + n], [nxt])[0]))
+    fw = [m.fast_weights(0, i) for i in range(shape.n_trainable)]
+    pos = m.position
+    m.close()
+    return losses, fw, pos
+
+
+def check(shape, tokens, name):
+    blob = weight_blob(shape)
+    cfg = O.Config.from_shape(shape)
+    P = O.unpack(blob, cfg)
+    ref_losses, Pf = O.run_sequence(cfg, P, tokens, shape.eta)
+    losses, fw, pos = run_gpu(shape, tokens, blob)
+    assert pos == len(tokens)
+    tl, tw = TOL[shape.compute]
+    lr = [abs(a - b) / abs(b) for a, b in zip(losses, ref_losses)]
+    print(f"\n{name}: loss rel err max {max(lr):.2e}; losses gpu {np.round(losses, 5)} ref {np.round(ref_losses, 5)}")
+    assert max(lr) < tl, (losses, ref_losses)
+    L, S = shape.n_layers, shape.n_trainable
+    for i in range(S):
+        l = L - S + i
+        for w, key in zip(fw[i], (f"W_up.{l}", f"W_down.{l}")):
+            e = rel(w, Pf[key])
+            dw = rel(w - P[key], Pf[key] - P[key])
+            print(f"  {key}: rel Frobenius {e:.2e}  update rel err {dw:.2e}")
+            assert e < tw, key
+
+
+def test_tiny_fp32_full_sequence():
+    s = SHAPES["tiny"]
+    check(s, sequence_tokens(s), "tiny fp32")
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_small_shapes(name):
+    s = SMALL[name]
+    check(s, zipf_tokens(s.seq_len, s.vocab, seed=1000), name)
+
+
+def test_eta0_matches_frozen_forward():
+    s = SMALL["dh64"].replace(eta=0.0)
+    tok = zipf_tokens(s.seq_len, s.vocab, seed=1001)
+    cfg = O.Config.from_shape(s)
+    P = O.unpack(weight_blob(s), cfg)
+    ref = O.dense_forward_losses(cfg, P, tok)
+    losses, fw, _ = run_gpu(s, tok, weight_blob(s))
+    assert max(abs(a - b) / b for a, b in zip(losses, ref)) < 2e-2
+    for i in range(s.n_trainable):
+        l = s.n_layers - s.n_trainable + i
+        assert np.array_equal(fw[i][0], P[f"W_up.{l}"].astype(np.float32))
+
+
+def test_bad_token_rejected_and_state_errors():
+    s = SMALL["dh64"]
+    m = T.TTT.from_shape(s)
+    with pytest.raises(T.TTTError) as e:
+        m.prefill_chunk(np.zeros(4, np.int32), [-1])
+    assert e.value.code == T.TTT_ERR_STATE
+    m.load_weights(weight_blob(s))
+    with pytest.raises(T.TTTError) as e:
+        m.prefill_chunk(np.array([1, 2, s.vocab], np.int32), [-1])
+    assert e.value.code == T.TTT_ERR_ARG
+    with pytest.raises(T.TTTError) as e:
+        m.prefill_chunk(np.zeros(s.chunk + 1, np.int32), [-1])
+    assert e.value.code == T.TTT_ERR_ARG
+    # the device path reports a bad id at the next sync
+    tok = torch.tensor([1, 2, s.vocab + 5], dtype=torch.int32, device="cuda")
+    nxt = torch.tensor([-1], dtype=torch.int32, device="cuda")
+    loss = torch.zeros(1, device="cuda")
+    m.prefill_chunk_dev(tok, 3, nxt, loss)
+    with pytest.raises(T.TTTError) as e:
+        m.sync()
+    assert e.value.code == T.TTT_ERR_DEVICE
+    m.close()
+
+
+def test_unsupported_shapes_rejected():
+    with pytest.raises(T.TTTError) as e:
+        T.TTT(T.make_config(4, 200, 4, 800, 512, 128, 64, 1e4, 0.0))      # d_head 50
+    assert e.value.code == T.TTT_ERR_UNSUPPORTED
+    with pytest.raises(T.TTTError) as e:
+        T.TTT(T.make_config(4, 256, 4, 1024, 512, 128, 256, 1e4, 0.0))     # k < b
+    assert e.value.code == T.TTT_ERR_ARG
