@@ -1,0 +1,331 @@
+#!/usr/bin/env python
+"""TTT-E2E inner-loop prefill throughput on B300 (libttt, sm_103a).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 760m] [--impl ours|reference]
+
+One step = one whole sequence through the inner loop: for every chunk of b
+tokens, forward through all blocks, next-token cross-entropy, backward through
+the last quarter of the blocks and the SGD step on their MLP weights, then the
+window-cache commit.  Each step restarts the sequence from the loaded weights
+(ttt_reset, inside the timed region).  value = tokens of all ranks / max over
+ranks of the device time of K steps (CUDA events on the library's stream).
+
+Multi-GPU: the inner loop is a serial chain within a sequence, so ranks are
+independent replicas (one sequence each, seed 1000 + rank); the only
+collectives are the timing barrier and the max-reduction of the elapsed time.
+
+--impl reference times the float64 oracle (the method as written, numpy) on
+the host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from ttt_inputs import SHAPES, sequence_tokens, weight_blob  # noqa: E402
+
+METRIC = "TTT prefill tokens/sec at 1 B300; % of bf16 tensor-core roofline"
+UNIT = "tokens/s"
+DATA = "synthetic: Zipf(1.1) token ids with repeated 32-token spans (seed 1000+rank), N(0,0.02) weights (seed 0)"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return dict(hbm=j["hbm_gbs"], tc=j["bf16_tflops"], tc_sus=j["bf16_tflops_sustained"], kind="measured")
+    return dict(hbm=6400.0, tc=1800.0, tc_sus=1400.0, kind="fallback")
+
+
+def algorithmic_flops(s, T):
+    """FLOPs the method needs for one T-token sequence (no recompute, no masked tiles).
+
+    forward : T L (8d^2 + 4df) + 4d P L + 2dVT, P = sum_p min(p+1, k) window pairs
+    backward: 2dVT (LM-head dX) + T (S-1)(8d^2 + 8df) + 6 T d f (first trainable block:
+              dU, dW_down, dW_up only) + (S-1)(4d P + 4d O), O = own-chunk causal pairs
+    """
+    d, f, V, L, S, k, b = s.d_model, s.d_ff, s.vocab, s.n_layers, s.n_trainable, s.window, s.chunk
+    pairs = sum(min(p + 1, k) for p in range(T)) if T <= k else k * (k + 1) // 2 + (T - k) * k
+    own = sum(n * (n + 1) // 2 for n in [min(b, T - c) for c in range(0, T, b)])
+    fwd = T * L * (8 * d * d + 4 * d * f) + 4 * d * pairs * L + 2 * d * V * T
+    bwd = (2 * d * V * T + T * (S - 1) * (8 * d * d + 8 * d * f) + T * 6 * d * f
+           + (S - 1) * (4 * d * pairs + 4 * d * own))
+    return fwd + bwd
+
+
+class Clocks:
+    """nvidia-smi sampler (200 ms) over the timed region."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                       "-lms", "200", "-i", str(gpu_id)], stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        try:
+            self.p.wait(5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = [[x.strip() for x in r.split(",")] for r in self.f.read().strip().splitlines() if r.count(",") >= 7]
+        os.unlink(self.f.name)
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [v for v in (num(r[0]) for r in rows) if v is not None]
+        mx = [v for v in (num(r[1]) for r in rows) if v is not None]
+        pw = [v for v in (num(r[2]) for r in rows) if v is not None]
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(sm), "power_w_max": max(pw) if pw else None}
+
+
+def cpu_sample(shape, blob, tokens, n_tok):
+    """Time the oracle on the first n_tok tokens (one inner-loop step) on the host cores."""
+    from oracle import ttt_oracle as O
+    try:
+        from threadpoolctl import threadpool_info
+        cores = max((i.get("num_threads", 1) for i in threadpool_info()), default=os.cpu_count())
+    except Exception:
+        cores = os.cpu_count()
+    cfg = O.Config.from_shape(shape.replace(chunk=n_tok))
+    P = O.unpack(blob, cfg)
+    ids = np.asarray(tokens[:n_tok])
+    tgt = O.chunk_targets(tokens, 0, n_tok)
+    t0 = time.perf_counter()
+    O.ttt_step(cfg, P, O.init_state(cfg), ids, tgt, shape.eta)
+    dt = time.perf_counter() - t0
+    return n_tok / dt, cores, dt
+
+
+def workload_name(s):
+    return (f"{s.n_layers}L d{s.d_model} H{s.n_heads} f{s.d_ff} V{s.vocab} k{s.window} b{s.chunk} "
+            f"theta{s.rope_theta:g} eta{s.eta:g} {s.compute}: {s.n_seqs} x {s.seq_len} tokens")
+
+
+def run_reference(a):
+    if int(os.environ.get("RANK", "0")) != 0:
+        return 0
+    shape = SHAPES[a.workload]
+    tokens = sequence_tokens(shape, 0)
+    blob = weight_blob(shape)
+    n_tok = a.cpu_tokens
+    for _ in range(a.warmup):
+        cpu_sample(shape, blob, tokens, n_tok)
+    secs, cores = [], None
+    for _ in range(a.steps):
+        _, cores, dt = cpu_sample(shape, blob, tokens, n_tok)
+        secs.append(dt)
+    value = a.steps * n_tok / sum(secs)
+    sample = f"first {n_tok} tokens of sequence 0 as one inner-loop step (forward, loss, suffix backward, SGD)"
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": a.gpus,
+           "steps": a.steps, "warmup": a.warmup, "ms_per_step": 1e3 * sum(secs) / a.steps,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": DATA,
+           "config": {"workload": workload_name(shape), "sample": sample},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+    return 0
+
+
+def run_ours(a):
+    import torch
+    import test_long_context_02_b300 as T
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    shape = SHAPES[a.workload].replace(n_seqs=1)
+    if a.tokens:
+        shape = shape.replace(seq_len=a.tokens)
+    Tn, b = shape.seq_len, shape.chunk
+    nc = math.ceil(Tn / b)
+    tokens = sequence_tokens(shape, rank)
+    blob = weight_blob(shape)
+    stream = torch.cuda.Stream()
+    m = T.TTT.from_shape(shape, stream=stream.cuda_stream)
+    m.load_weights(blob)
+    d_tok = torch.tensor(tokens, dtype=torch.int32, device="cuda")
+    d_loss = torch.zeros(nc, dtype=torch.float32, device="cuda")
+
+    def one_step():
+        m.reset()
+        m.prefill_sequence_dev(d_tok, Tn, d_loss)
+
+    for _ in range(a.warmup):
+        one_step()
+    m.sync()
+
+    # ---------------------------------------------------------------- timed region
+    clocks = Clocks(f"GPU-{torch.cuda.get_device_properties(local).uuid}")
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    m.profile(True)
+    barrier()
+    torch.cuda.synchronize()
+    l0 = m.launches
+    ev0.record(stream)
+    for _ in range(a.steps):
+        one_step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    launches = m.launches - l0
+    ms = ev0.elapsed_time(ev1)
+    clk = clocks.stop()
+    prof = m.profile_read()
+    m.profile(False)
+    m.sync()
+    losses = d_loss.cpu().numpy()
+    if not np.all(np.isfinite(losses)):
+        raise RuntimeError(f"non-finite chunk losses: {losses}")
+
+    # one unprofiled step, for the cost of the event bracketing
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    one_step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms_unprof = ev0.elapsed_time(ev1)
+
+    ms_max = ms
+    if dist is not None:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+
+    # ------------------------------------------------------------ end-to-end (host buffers)
+    e2e_steps = max(1, min(a.steps, 2))
+    pin_tok = torch.tensor(tokens, dtype=torch.int32).pin_memory()
+    nxt = np.array([tokens[s + b] if s + b < Tn else -1 for s in range(0, Tn, b)], np.int32)
+    pin_next = torch.tensor(nxt).pin_memory()
+    pin_loss = torch.zeros(nc, dtype=torch.float32).pin_memory()
+    base_t, base_n, base_l = pin_tok.data_ptr(), pin_next.data_ptr(), pin_loss.data_ptr()
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        m.reset()
+        for ci in range(nc):
+            s0 = ci * b
+            n = min(b, Tn - s0)
+            m._check(T.ttt_prefill_chunk(m._h, base_t + 4 * s0, n, base_n + 4 * ci, base_l + 4 * ci),
+                     "ttt_prefill_chunk")
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    if dist is not None:
+        t = torch.tensor([e2e_s], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    barrier()
+
+    # --------------------------------------------------------------- reporting (rank 0)
+    pk = peaks()
+    alg = algorithmic_flops(shape, Tn)
+    value = world * a.steps * Tn / (ms_max / 1e3)
+    tc_frac = alg * a.steps / (ms / 1e3) / (pk["tc_sus"] * 1e12)
+    total_ms = sum(v["ms"] for v in prof.values())
+    dom_name, dom = max(prof.items(), key=lambda kv: kv[1]["ms"])
+    avg_launch_ms = dom["ms"] / dom["launches"]
+    if dom["alg_flops"] > 0:
+        ach = dom["alg_flops"] / (dom["ms"] / 1e3) / 1e12
+        roof = {"kernel": dom_name, "bound": "tensor", "achieved": ach, "peak": pk["tc_sus"], "unit": "TFLOP/s",
+                "frac": ach / pk["tc_sus"], "traffic": None,
+                "peak_source": f"bf16_tflops_sustained ({pk['kind']}); burst {pk['tc']}",
+                "frac_of_burst": ach / pk["tc"], "avg_launch_ms": avg_launch_ms,
+                "alg_flops_per_launch": dom["alg_flops"] / dom["launches"]}
+    else:
+        ach = dom["bytes"] / (dom["ms"] / 1e3) / 1e9
+        roof = {"kernel": dom_name, "bound": "hbm", "achieved": ach, "peak": pk["hbm"], "unit": "GB/s",
+                "frac": ach / pk["hbm"], "traffic": None, "avg_launch_ms": avg_launch_ms}
+    kernels = {k: {"ms_per_step": round(v["ms"] / a.steps, 3), "share": round(v["ms"] / total_ms, 4),
+                   "launches_per_step": v["launches"] // a.steps,
+                   "alg_tflops": round(v["alg_flops"] / (v["ms"] / 1e3) / 1e12, 1) if v["alg_flops"] else None,
+                   "exec_tflops": round(v["exec_flops"] / (v["ms"] / 1e3) / 1e12, 1) if v["exec_flops"] else None,
+                   "hbm_gbs": round(v["bytes"] / (v["ms"] / 1e3) / 1e9, 1) if v["bytes"] else None}
+               for k, v in sorted(prof.items(), key=lambda kv: -kv[1]["ms"])}
+    if rank != 0:
+        m.close()
+        return 0
+    out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
+           "ms_per_step": ms_max / a.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": "bf16" if shape.compute == "bf16" else "f32", "data": DATA,
+           "config": {"workload": workload_name(shape), "tokens_per_step_per_gpu": Tn, "chunks": nc,
+                      "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                      "l2": "working set larger than L2 (bf16 weights + window cache > 2 GB), no flush",
+                      "timing": "CUDA events on the library stream; per-class event bracketing on",
+                      "unprofiled_ms_per_step": ms_unprof,
+                      "alg_gflop_per_token": alg / Tn / 1e9},
+           "tc_roofline_frac": tc_frac,
+           "tc_roofline_frac_of_burst": tc_frac * pk["tc_sus"] / pk["tc"],
+           "roofline": roof, "kernels": kernels, "clocks": clk, "gpu_launches": launches,
+           "e2e": {"value": world * e2e_steps * Tn / e2e_s, "unit": UNIT, "h2d_bytes_per_step": 4 * Tn + 4 * nc,
+                   "d2h_bytes_per_step": 4 * nc, "api": "ttt_prefill_chunk per chunk, pinned host buffers"},
+           "final_chunk_loss": float(losses[-1])}
+    if world == 1 and not a.no_cpu_baseline:
+        v, cores, dt = cpu_sample(shape, blob, tokens, a.cpu_tokens)
+        out["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                               "sample": f"first {a.cpu_tokens} tokens as one inner-loop step, {dt:.1f} s"}
+    print(json.dumps(out), flush=True)
+    m.close()
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="760m", choices=sorted(SHAPES))
+    ap.add_argument("--tokens", type=int, default=0, help="override the sequence length (smoke runs)")
+    ap.add_argument("--cpu-tokens", type=int, default=128, help="oracle sample size (tokens)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    a = ap.parse_args()
+    if a.warmup < 3:
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    return run_reference(a) if a.impl == "reference" else run_ours(a)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

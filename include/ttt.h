@@ -128,6 +128,37 @@ TTT_API int ttt_sync(ttt_ctx* ctx);
  */
 TTT_API int ttt_get_fast_weights(ttt_ctx* ctx, int32_t seq, int32_t suffix_layer, float* w_up, float* w_down);
 
+/*
+ * Restart every sequence from the loaded weights without re-uploading them:
+ * position 0, empty window cache, fast weights = the loaded W_up / W_down.
+ * Enqueued on the context stream.
+ */
+TTT_API int ttt_reset(ttt_ctx* ctx);
+
+/* Kernels launched by this context since it was created (monotonic counter). */
+TTT_API int64_t ttt_launch_count(const ttt_ctx* ctx);
+
+/*
+ * Per-kernel-class timing.  ttt_profile(ctx, 1) synchronises, clears the
+ * accumulators and starts bracketing every launch with CUDA events on the
+ * context stream; ttt_profile(ctx, 0) stops.  ttt_profile_read synchronises,
+ * folds the recorded launches into the accumulators and writes up to max_out
+ * entries (classes with at least one launch); *n_out = number of such classes.
+ * alg_flops counts the multiply-adds the method needs (x2), exec_flops what the
+ * kernels execute (masked attention tiles, logit recompute, split-mode triple
+ * products), bytes the algorithmic HBM traffic of memory-bound classes.
+ */
+typedef struct {
+  char name[32];
+  int64_t launches;
+  double ms;
+  double alg_flops;
+  double exec_flops;
+  double bytes;
+} ttt_kernel_stat;
+TTT_API int ttt_profile(ttt_ctx* ctx, int enable);
+TTT_API int ttt_profile_read(ttt_ctx* ctx, ttt_kernel_stat* out, int max_out, int* n_out);
+
 /* Current absolute position (tokens consumed) of every sequence. */
 TTT_API int64_t ttt_position(const ttt_ctx* ctx);
 

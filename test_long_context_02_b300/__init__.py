@@ -16,7 +16,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libttt.so")
 
 if not os.path.exists(LIB_PATH):
-    raise ImportError(f"{LIB_PATH} is missing: build it with `python -m test_long_context_02_b300.build` "
+    raise ImportError(f"{LIB_PATH} is missing: build it with `python test_long_context_02_b300/build.py` "
                       "(there is no fallback implementation)")
 lib = ctypes.CDLL(LIB_PATH)
 
@@ -117,6 +117,18 @@ ttt_get_fast_weights = _sig("ttt_get_fast_weights", ctypes.c_int, _vp, _i32, _i3
 ttt_position = _sig("ttt_position", _i64, _vp)
 ttt_destroy = _sig("ttt_destroy", None, _vp)
 ttt_last_error = _sig("ttt_last_error", ctypes.c_char_p, _vp)
+ttt_reset = _sig("ttt_reset", ctypes.c_int, _vp)
+ttt_launch_count = _sig("ttt_launch_count", _i64, _vp)
+
+
+class ttt_kernel_stat(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 32), ("launches", _i64), ("ms", ctypes.c_double),
+                ("alg_flops", ctypes.c_double), ("exec_flops", ctypes.c_double), ("bytes", ctypes.c_double)]
+
+
+ttt_profile = _sig("ttt_profile", ctypes.c_int, _vp, ctypes.c_int)
+ttt_profile_read = _sig("ttt_profile_read", ctypes.c_int, _vp, ctypes.POINTER(ttt_kernel_stat), ctypes.c_int,
+                        ctypes.POINTER(ctypes.c_int))
 
 
 def attn_fwd(n, H, dh, window, pos0, q, kc, vc, ko, vo, o, lse=None, *, split=False, lo=None, err=None,
@@ -208,6 +220,25 @@ class TTT:
         self._check(ttt_get_fast_weights(self._h, seq, suffix_layer, up.ctypes.data, down.ctypes.data),
                     "ttt_get_fast_weights")
         return up, down
+
+    def reset(self):
+        self._check(ttt_reset(self._h), "ttt_reset")
+
+    @property
+    def launches(self) -> int:
+        return int(ttt_launch_count(self._h))
+
+    def profile(self, enable: bool):
+        self._check(ttt_profile(self._h, int(enable)), "ttt_profile")
+
+    def profile_read(self):
+        """{class name: dict(launches, ms, alg_flops, exec_flops, bytes)} since ttt_profile(1)."""
+        arr = (ttt_kernel_stat * 64)()
+        n = ctypes.c_int()
+        self._check(ttt_profile_read(self._h, arr, 64, ctypes.byref(n)), "ttt_profile_read")
+        return {arr[i].name.decode(): dict(launches=arr[i].launches, ms=arr[i].ms, alg_flops=arr[i].alg_flops,
+                                           exec_flops=arr[i].exec_flops, bytes=arr[i].bytes)
+                for i in range(min(n.value, 64))}
 
     @property
     def position(self) -> int:

@@ -1,6 +1,6 @@
 """Build libttt.so in-tree with nvcc for sm_103a (B300).
 
-    python -m test_long_context_02_b300.build [-v] [-j N]
+    python test_long_context_02_b300/build.py [-v] [-j N] [--ptxas-v]
 
 Each csrc/*.cu is compiled to _build/<name>.o (skipped when newer than its
 sources and every header), then linked into test_long_context_02_b300/libttt.so.

@@ -41,6 +41,7 @@ struct AttnBwdMaps {
   CUtensorMap dO, dOl; // output gradient [n][d]
 };
 
-int attn_bwd_run(const AttnBwdMaps& m, const AttnBwdArgs& a, bool split, cudaStream_t st);
+// which: 0 = both kernels, 1 = dQ only, 2 = dK/dV only
+int attn_bwd_run(const AttnBwdMaps& m, const AttnBwdArgs& a, bool split, cudaStream_t st, int which = 0);
 
 }  // namespace ttt

@@ -557,7 +557,7 @@ __global__ void __launch_bounds__(192, 1)
 }
 
 template <int DH, bool SPLIT>
-int launch_bwd(const AttnBwdMaps& m, const AttnBwdArgs& a, cudaStream_t st) {
+int launch_bwd(const AttnBwdMaps& m, const AttnBwdArgs& a, cudaStream_t st, int which) {
   using C = BCfg<DH, SPLIT>;
   auto kq = attn_dq_kernel<DH, SPLIT>;
   auto kkv = attn_dkv_kernel<DH, SPLIT>;
@@ -570,29 +570,31 @@ int launch_bwd(const AttnBwdMaps& m, const AttnBwdArgs& a, cudaStream_t st) {
   }
   dim3 grid((a.g.n + 127) / 128, a.g.H);
   const AttnMaps& f = m.f;
-  kq<<<grid, 192, C::SMEM, st>>>(f.q, f.ql, m.dO, m.dOl, f.kr, f.krl, f.vr, f.vrl, f.ko, f.kol, f.vo, f.vol, a);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return (int)e;
-  kkv<<<grid, 192, C::XSMEM, st>>>(f.q, f.ql, m.dO, m.dOl, f.ko, f.kol, f.vo, f.vol, a);
+  if (which != 2) {
+    kq<<<grid, 192, C::SMEM, st>>>(f.q, f.ql, m.dO, m.dOl, f.kr, f.krl, f.vr, f.vrl, f.ko, f.kol, f.vo, f.vol, a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return (int)e;
+  }
+  if (which != 1) kkv<<<grid, 192, C::XSMEM, st>>>(f.q, f.ql, m.dO, m.dOl, f.ko, f.kol, f.vo, f.vol, a);
   return (int)cudaGetLastError();
 }
 
 }  // namespace
 
-int attn_bwd_run(const AttnBwdMaps& m, const AttnBwdArgs& a, bool split, cudaStream_t st) {
+int attn_bwd_run(const AttnBwdMaps& m, const AttnBwdArgs& a, bool split, cudaStream_t st, int which) {
   if (a.g.n <= 0) return 0;
   if (split) {
     switch (a.g.dh) {
-      case 32: return launch_bwd<32, true>(m, a, st);
-      case 64: return launch_bwd<64, true>(m, a, st);
+      case 32: return launch_bwd<32, true>(m, a, st, which);
+      case 64: return launch_bwd<64, true>(m, a, st, which);
     }
     return (int)cudaErrorInvalidValue;
   }
   switch (a.g.dh) {
-    case 32: return launch_bwd<32, false>(m, a, st);
-    case 64: return launch_bwd<64, false>(m, a, st);
-    case 96: return launch_bwd<96, false>(m, a, st);
-    case 128: return launch_bwd<128, false>(m, a, st);
+    case 32: return launch_bwd<32, false>(m, a, st, which);
+    case 64: return launch_bwd<64, false>(m, a, st, which);
+    case 96: return launch_bwd<96, false>(m, a, st, which);
+    case 128: return launch_bwd<128, false>(m, a, st, which);
   }
   return (int)cudaErrorInvalidValue;
 }

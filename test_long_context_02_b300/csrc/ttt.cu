@@ -82,7 +82,27 @@ struct ttt_ctx {
   float2* part = nullptr;
   float *dy = nullptr, *dxn = nullptr, *dh32 = nullptr, *D = nullptr, *dq = nullptr, *dk = nullptr, *dv = nullptr;
   Pair dy16, da, dh16, do16, dqkv;
+  // initial fast weights (device copy) for ttt_reset
+  float *init_up = nullptr, *init_down = nullptr;
+  // launch counting and optional per-class event timing
+  int64_t launches = 0;
+  bool prof_on = false;
+  std::vector<cudaEvent_t> ev_pool;
+  size_t ev_used = 0;
+  struct ProfRec {
+    int cls;
+    cudaEvent_t a, b;
+    double alg, exec, bytes;
+    int nkern;
+  };
+  std::vector<ProfRec> recs;
+  struct ProfAcc {
+    int64_t launches = 0;
+    double ms = 0, alg = 0, exec = 0, bytes = 0;
+  };
+  std::vector<ProfAcc> acc;
 };
+using ProfRec = ttt_ctx::ProfRec;
 
 namespace {
 
@@ -147,6 +167,55 @@ bool attn_maps(AttnMaps* m, const Pair& q, const Pair& kr, const Pair& vr, const
   return ok;
 }
 
+// Kernel classes timed by the optional profiler (names exported by ttt_profile_read).
+enum Cls : int {
+  K_GEMM_QKV, K_ATTN_FWD, K_GEMM_O, K_GEMM_UP, K_GEMM_DOWN, K_CE_FWD, K_CE_BWD, K_LM_DX, K_MLP_DX, K_DW_SGD,
+  K_ATTN_DX, K_ATTN_DQ, K_ATTN_DKV, K_RMSNORM, K_ROPE, K_COMMIT, K_MISC, K_NCLS
+};
+const char* const kClsName[K_NCLS] = {
+    "gemm_qkv", "attn_fwd", "gemm_o_resid", "gemm_up_gelu", "gemm_down_resid", "lmhead_ce_fwd",
+    "lmhead_ce_bwd", "lmhead_dx", "gemm_mlp_dx", "gemm_dw_sgd", "gemm_attn_dx", "attn_bwd_dq",
+    "attn_bwd_dkv", "rmsnorm", "rope", "kv_commit", "misc"};
+
+cudaEvent_t next_event(ttt_ctx* c) {
+  if (c->ev_used == c->ev_pool.size()) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    c->ev_pool.push_back(e);
+  }
+  return c->ev_pool[c->ev_used++];
+}
+
+// Run one launch site: count its kernels and, when profiling, bracket it with events.
+template <class F>
+int site(ttt_ctx* c, int cls, int nkern, double alg, double exec, double bytes, F&& f) {
+  cudaEvent_t a = nullptr;
+  if (c->prof_on && (a = next_event(c))) cudaEventRecord(a, c->st);
+  const int r = f();
+  if (a) {
+    cudaEvent_t b = next_event(c);
+    if (b) {
+      cudaEventRecord(b, c->st);
+      c->recs.push_back(ProfRec{cls, a, b, alg, exec, bytes, nkern});
+    }
+  }
+  c->launches += nkern;
+  return r;
+}
+
+#define RUN(cls, nk, alg, exec, bytes, expr) CK(site(c, cls, nk, alg, exec, bytes, [&]() { return (int)(expr); }))
+
+// Tiles of 128 keys visited by the attention kernels for query tile qt (as the kernels enumerate them).
+long attn_tiles(long pos0, int n, int k, int qt) {
+  long ring = 0;
+  if (pos0 > 0) {
+    const long lo = std::max(0L, pos0 + 128L * qt - k + 1);
+    ring = (pos0 - 1) / 128 - lo / 128 + 1;
+  }
+  const int qend = std::min(n, 128 * qt + 128);
+  return ring + (qend - 1) / 128 + 1;
+}
+
 // One inner-loop step of sequence s: tokens tok[n] / next target next[1] on the device.
 int step(ttt_ctx* c, int s, const int* tok, int n, const int* next, float* loss_out) {
   Seq& sq_ = c->seqs[s];
@@ -156,10 +225,21 @@ int step(ttt_ctx* c, int s, const int* tok, int n, const int* next, float* loss_
   const bool sp = c->split;
   const int P0 = L - S;  // first trainable block
   const float eta = c->cfg.eta;
+  const double nn = n, dd = d, ff = f, VV = V;
+  const double ops = sp ? 3.0 : 1.0;             // products per multiply in split mode
+  const double eb = sp ? 4.0 : 2.0;              // bytes per operand element (hi [+ lo])
 
-  CK(rows_targets(tok, n, next, V, c->tgt, c->derr, st));
-  CK(rows_embed(tok, n, c->E, V, d, c->x, c->derr, st));
-  CK(rows_rope_table(pos0, n, dh, c->inv_freq, c->cs, c->sn, st));
+  // algorithmic work of this chunk's attention: window pairs and own-chunk causal pairs
+  double pairs = 0, tile_pairs = 0;
+  for (long p = pos0; p < pos0 + n; ++p) pairs += (double)std::min<long>(p + 1, k);
+  const double own_pairs = nn * (nn + 1) / 2;
+  for (int qt = 0; qt < (n + 127) / 128; ++qt) tile_pairs += 128.0 * 128.0 * attn_tiles(pos0, n, k, qt);
+  const int nq = (n + 127) / 128;
+  const double own_tile_pairs = 128.0 * 128.0 * nq * (nq + 1) / 2;
+
+  RUN(K_MISC, 1, 0, 0, nn * 8, rows_targets(tok, n, next, V, c->tgt, c->derr, st));
+  RUN(K_MISC, 1, 0, 0, nn * dd * 8, rows_embed(tok, n, c->E, V, d, c->x, c->derr, st));
+  RUN(K_ROPE, 1, 0, 0, nn * dh * 4, rows_rope_table(pos0, n, dh, c->inv_freq, c->cs, c->sn, st));
 
   auto in_ptr = [&](int l) -> float* { return l >= P0 ? c->sx + (long)(l - P0) * b * d : c->x; };
 
@@ -190,15 +270,18 @@ int step(ttt_ctx* c, int s, const int* tok, int n, const int* next, float* loss_
     Pair ko = c->kown.at((long)l * b * d), vo = c->vown.at((long)l * b * d);
     Pair kr = sq_.ring_k.at((long)l * k * d), vr = sq_.ring_v.at((long)l * k * d);
 
-    CK(rows_rmsnorm(xin, c->gains + (long)(2 * l) * d, c->cfg.rms_eps, n, d, xn_a.hi, xn_a.lo,
-                    suf ? c->srs_a + (long)si * b : nullptr, st));
+    RUN(K_RMSNORM, 1, 0, 0, nn * dd * (4 + eb),
+        rows_rmsnorm(xin, c->gains + (long)(2 * l) * d, c->cfg.rms_eps, n, d, xn_a.hi, xn_a.lo,
+                     suf ? c->srs_a + (long)si * b : nullptr, st));
     {
       GemmArgs g;
       g.M = n; g.N = 3 * d; g.K = d;
       g.out32 = c->qkv; g.ldo32 = 3 * d; g.err = c->derr;
-      CK(gemm_run(EPI_F32, opnd(xn_a, d, 0), opnd(c->Wqkv.at((long)l * d * 3 * d), 3 * d, 1), g, sp, st));
+      RUN(K_GEMM_QKV, 1, 6 * nn * dd * dd, 6 * nn * dd * dd * ops, 0,
+          gemm_run(EPI_F32, opnd(xn_a, d, 0), opnd(c->Wqkv.at((long)l * d * 3 * d), 3 * d, 1), g, sp, st));
     }
-    CK(rows_rope_qkv(c->qkv, c->cs, c->sn, n, H, dh, qb.hi, qb.lo, ko.hi, ko.lo, vo.hi, vo.lo, st));
+    RUN(K_ROPE, 1, 0, 0, nn * dd * (12 + 3 * eb),
+        rows_rope_qkv(c->qkv, c->cs, c->sn, n, H, dh, qb.hi, qb.lo, ko.hi, ko.lo, vo.hi, vo.lo, st));
     {
       AttnMaps m;
       if (!attn_maps(&m, qb, kr, vr, ko, vo, n, d, k)) return fail(c, TTT_ERR_CUDA, "attention tensor maps");
@@ -206,43 +289,50 @@ int step(ttt_ctx* c, int s, const int* tok, int n, const int* next, float* loss_
       a2.o_hi = ob.hi;
       a2.o_lo = ob.lo;
       a2.lse = suf ? c->slse + (long)si * H * b : nullptr;
-      CK(attn_fwd_run(m, a2, sp, st));
+      RUN(K_ATTN_FWD, 1, 4 * dd * pairs, 4 * dd * tile_pairs * ops, 0, attn_fwd_run(m, a2, sp, st));
     }
     {
       GemmArgs g;
       g.M = n; g.N = d; g.K = d;
       g.out32 = hbuf; g.ldo32 = d; g.resid = xin; g.ldr = d; g.err = c->derr;
-      CK(gemm_run(EPI_RESID, opnd(ob, d, 0), opnd(c->Wo.at((long)l * d * d), d, 1), g, sp, st));
+      RUN(K_GEMM_O, 1, 2 * nn * dd * dd, 2 * nn * dd * dd * ops, 0,
+          gemm_run(EPI_RESID, opnd(ob, d, 0), opnd(c->Wo.at((long)l * d * d), d, 1), g, sp, st));
     }
-    CK(rows_rmsnorm(hbuf, c->gains + (long)(2 * l + 1) * d, c->cfg.rms_eps, n, d, xn_m.hi, xn_m.lo,
-                    suf ? c->srs_m + (long)si * b : nullptr, st));
+    RUN(K_RMSNORM, 1, 0, 0, nn * dd * (4 + eb),
+        rows_rmsnorm(hbuf, c->gains + (long)(2 * l + 1) * d, c->cfg.rms_eps, n, d, xn_m.hi, xn_m.lo,
+                     suf ? c->srs_m + (long)si * b : nullptr, st));
     {
       GemmArgs g;
       g.M = n; g.N = f; g.K = d;
       g.out32 = abuf; g.ldo32 = f; g.oh = ub.hi; g.ol = ub.lo; g.ldo = f; g.err = c->derr;
       Pair w = suf ? sq_.up16.at((long)si * d * f) : c->Wup.at((long)l * d * f);
-      CK(gemm_run(EPI_GELU, opnd(xn_m, d, 0), opnd(w, f, 1), g, sp, st));
+      RUN(K_GEMM_UP, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 0,
+          gemm_run(EPI_GELU, opnd(xn_m, d, 0), opnd(w, f, 1), g, sp, st));
     }
     {
       GemmArgs g;
       g.M = n; g.N = d; g.K = f;
       g.out32 = xout; g.ldo32 = d; g.resid = hbuf; g.ldr = d; g.err = c->derr;
       Pair w = suf ? sq_.down16.at((long)si * f * d) : c->Wdown.at((long)l * f * d);
-      CK(gemm_run(EPI_RESID, opnd(ub, f, 0), opnd(w, d, 1), g, sp, st));
+      RUN(K_GEMM_DOWN, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 0,
+          gemm_run(EPI_RESID, opnd(ub, f, 0), opnd(w, d, 1), g, sp, st));
     }
   }
   // final norm + LM head + cross-entropy statistics
-  CK(rows_rmsnorm(c->x, c->gains + (long)(2 * L) * d, c->cfg.rms_eps, n, d, c->xf.hi, c->xf.lo, c->rs_f, st));
+  RUN(K_RMSNORM, 1, 0, 0, nn * dd * (4 + eb),
+      rows_rmsnorm(c->x, c->gains + (long)(2 * L) * d, c->cfg.rms_eps, n, d, c->xf.hi, c->xf.lo, c->rs_f, st));
   const int bn = pick_bn(n, V);
   const int ntiles = (V + bn - 1) / bn;
   {
     GemmArgs g;
     g.M = n; g.N = V; g.K = d;
     g.tgt = c->tgt; g.part = c->part; g.zt = c->zt; g.err = c->derr;
-    CK(gemm_run(EPI_CE_FWD, opnd(c->xf, d, 0), opnd(c->Wlm, V, 1), g, sp, st));
+    RUN(K_CE_FWD, 1, 2 * nn * dd * VV, 2 * nn * dd * VV * ops, 0,
+        gemm_run(EPI_CE_FWD, opnd(c->xf, d, 0), opnd(c->Wlm, V, 1), g, sp, st));
   }
-  CK(rows_ce_combine(c->part, c->zt, c->tgt, n, ntiles, c->lse_row, c->loss_row, st));
-  CK(rows_loss_mean(c->loss_row, c->tgt, n, loss_out, c->inv_nvalid, st));
+  RUN(K_MISC, 1, 0, 0, nn * ntiles * 8,
+      rows_ce_combine(c->part, c->zt, c->tgt, n, ntiles, c->lse_row, c->loss_row, st));
+  RUN(K_MISC, 1, 0, 0, nn * 8, rows_loss_mean(c->loss_row, c->tgt, n, loss_out, c->inv_nvalid, st));
 
   // ----------------------------------------------------------------- backward
   {  // dZ = (softmax(Z) - onehot(target)) / n_valid, logits recomputed tile by tile
@@ -250,16 +340,19 @@ int step(ttt_ctx* c, int s, const int* tok, int n, const int* next, float* loss_
     g.M = n; g.N = V; g.K = d;
     g.tgt = c->tgt; g.lse = c->lse_row; g.scale_dev = c->inv_nvalid;
     g.oh = c->dz.hi; g.ol = c->dz.lo; g.ldo = V; g.err = c->derr;
-    CK(gemm_run(EPI_CE_BWD, opnd(c->xf, d, 0), opnd(c->Wlm, V, 1), g, sp, st));
+    RUN(K_CE_BWD, 1, 0, 2 * nn * dd * VV * ops, 0,
+        gemm_run(EPI_CE_BWD, opnd(c->xf, d, 0), opnd(c->Wlm, V, 1), g, sp, st));
   }
   {
     GemmArgs g;
     g.M = n; g.N = d; g.K = V;
     g.out32 = c->dxn; g.ldo32 = d; g.err = c->derr;
-    CK(gemm_run(EPI_F32, opnd(c->dz, V, 0), opnd(c->Wlm, V, 0), g, sp, st));
+    RUN(K_LM_DX, 1, 2 * nn * dd * VV, 2 * nn * dd * VV * ops, 0,
+        gemm_run(EPI_F32, opnd(c->dz, V, 0), opnd(c->Wlm, V, 0), g, sp, st));
   }
-  CK(rows_rmsnorm_bwd(c->dxn, c->x, c->gains + (long)(2 * L) * d, c->rs_f, nullptr, n, d, c->dy, c->dy16.hi,
-                      c->dy16.lo, st));
+  RUN(K_RMSNORM, 1, 0, 0, nn * dd * (12 + eb),
+      rows_rmsnorm_bwd(c->dxn, c->x, c->gains + (long)(2 * L) * d, c->rs_f, nullptr, n, d, c->dy, c->dy16.hi,
+                       c->dy16.lo, st));
   for (int si = S - 1; si >= 0; --si) {
     const int l = P0 + si;
     Pair up16 = sq_.up16.at((long)si * d * f), down16 = sq_.down16.at((long)si * f * d);
@@ -268,40 +361,47 @@ int step(ttt_ctx* c, int s, const int* tok, int n, const int* next, float* loss_
       g.M = n; g.N = f; g.K = d;
       g.aux = c->sa + (long)si * b * f; g.ldaux = f;
       g.oh = c->da.hi; g.ol = c->da.lo; g.ldo = f; g.err = c->derr;
-      CK(gemm_run(EPI_GELU_BWD, opnd(c->dy16, d, 0), opnd(down16, d, 0), g, sp, st));
+      RUN(K_MLP_DX, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 0,
+          gemm_run(EPI_GELU_BWD, opnd(c->dy16, d, 0), opnd(down16, d, 0), g, sp, st));
     }
     {  // W_down -= eta U^T dY
       GemmArgs g;
       g.M = f; g.N = d; g.K = n;
       g.w32 = sq_.down32 + (long)si * f * d; g.wh = down16.hi; g.wl = down16.lo; g.ldw = d; g.eta = eta;
       g.err = c->derr;
-      CK(gemm_run(EPI_SGD, opnd(c->su.at((long)si * b * f), f, 1), opnd(c->dy16, d, 1), g, sp, st));
+      RUN(K_DW_SGD, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 8 * dd * ff,
+          gemm_run(EPI_SGD, opnd(c->su.at((long)si * b * f), f, 1), opnd(c->dy16, d, 1), g, sp, st));
     }
     if (si > 0) {  // dXn_m = dA W_up^T  (before W_up changes)
       GemmArgs g;
       g.M = n; g.N = d; g.K = f;
       g.out32 = c->dxn; g.ldo32 = d; g.err = c->derr;
-      CK(gemm_run(EPI_F32, opnd(c->da, f, 0), opnd(up16, f, 0), g, sp, st));
+      RUN(K_MLP_DX, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 0,
+          gemm_run(EPI_F32, opnd(c->da, f, 0), opnd(up16, f, 0), g, sp, st));
     }
     {  // W_up -= eta Xn_m^T dA
       GemmArgs g;
       g.M = d; g.N = f; g.K = n;
       g.w32 = sq_.up32 + (long)si * d * f; g.wh = up16.hi; g.wl = up16.lo; g.ldw = f; g.eta = eta;
       g.err = c->derr;
-      CK(gemm_run(EPI_SGD, opnd(c->sxm.at((long)si * b * d), d, 1), opnd(c->da, f, 1), g, sp, st));
+      RUN(K_DW_SGD, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 8 * dd * ff,
+          gemm_run(EPI_SGD, opnd(c->sxm.at((long)si * b * d), d, 1), opnd(c->da, f, 1), g, sp, st));
     }
     if (si == 0) break;  // the first trainable block's attention needs no gradient
     // dH = dY + RMSNorm_m^T(dXn_m)
-    CK(rows_rmsnorm_bwd(c->dxn, c->sh + (long)si * b * d, c->gains + (long)(2 * l + 1) * d, c->srs_m + (long)si * b,
-                        c->dy, n, d, c->dh32, c->dh16.hi, c->dh16.lo, st));
+    RUN(K_RMSNORM, 1, 0, 0, nn * dd * (20 + eb),
+        rows_rmsnorm_bwd(c->dxn, c->sh + (long)si * b * d, c->gains + (long)(2 * l + 1) * d,
+                         c->srs_m + (long)si * b, c->dy, n, d, c->dh32, c->dh16.hi, c->dh16.lo, st));
     {  // dO = dH Wo^T
       GemmArgs g;
       g.M = n; g.N = d; g.K = d;
       g.oh = c->do16.hi; g.ol = c->do16.lo; g.ldo = d; g.err = c->derr;
-      CK(gemm_run(EPI_OPND, opnd(c->dh16, d, 0), opnd(c->Wo.at((long)l * d * d), d, 0), g, sp, st));
+      RUN(K_ATTN_DX, 1, 2 * nn * dd * dd, 2 * nn * dd * dd * ops, 0,
+          gemm_run(EPI_OPND, opnd(c->dh16, d, 0), opnd(c->Wo.at((long)l * d * d), d, 0), g, sp, st));
     }
     Pair qb = c->sq.at((long)si * b * d), ob = c->so.at((long)si * b * d);
-    CK(rows_attn_rowdot(c->do16.hi, c->do16.lo, ob.hi, ob.lo, n, H, dh, c->D, st));
+    RUN(K_MISC, 1, 0, 0, nn * dd * 2 * eb,
+        rows_attn_rowdot(c->do16.hi, c->do16.lo, ob.hi, ob.lo, n, H, dh, c->D, st));
     {
       AttnBwdMaps m;
       Pair ko = c->kown.at((long)l * b * d), vo = c->vown.at((long)l * b * d);
@@ -324,30 +424,36 @@ int step(ttt_ctx* c, int s, const int* tok, int n, const int* next, float* loss_
       ba.dv = c->dv;
       ba.ldg = d;
       ba.scale = (float)(1.0 / std::sqrt((double)dh));
-      CK(attn_bwd_run(m, ba, sp, st));
+      RUN(K_ATTN_DQ, 1, 4 * dd * pairs, 6 * dd * tile_pairs * ops, 0, attn_bwd_run(m, ba, sp, st, 1));
+      RUN(K_ATTN_DKV, 1, 4 * dd * own_pairs, 8 * dd * own_tile_pairs * ops, 0, attn_bwd_run(m, ba, sp, st, 2));
     }
-    CK(rows_rope_bwd(c->dq, c->dk, c->dv, c->cs, c->sn, n, H, dh, c->dqkv.hi, c->dqkv.lo, st));
+    RUN(K_ROPE, 1, 0, 0, nn * dd * (12 + 3 * eb),
+        rows_rope_bwd(c->dq, c->dk, c->dv, c->cs, c->sn, n, H, dh, c->dqkv.hi, c->dqkv.lo, st));
     {  // dXn_a = dQKV Wqkv^T
       GemmArgs g;
       g.M = n; g.N = d; g.K = 3 * d;
       g.out32 = c->dxn; g.ldo32 = d; g.err = c->derr;
-      CK(gemm_run(EPI_F32, opnd(c->dqkv, 3 * d, 0), opnd(c->Wqkv.at((long)l * d * 3 * d), 3 * d, 0), g, sp, st));
+      RUN(K_ATTN_DX, 1, 6 * nn * dd * dd, 6 * nn * dd * dd * ops, 0,
+          gemm_run(EPI_F32, opnd(c->dqkv, 3 * d, 0), opnd(c->Wqkv.at((long)l * d * 3 * d), 3 * d, 0), g, sp, st));
     }
     // dY_{l-1} = dH + RMSNorm_a^T(dXn_a)
-    CK(rows_rmsnorm_bwd(c->dxn, c->sx + (long)si * b * d, c->gains + (long)(2 * l) * d, c->srs_a + (long)si * b,
-                        c->dh32, n, d, c->dy, c->dy16.hi, c->dy16.lo, st));
+    RUN(K_RMSNORM, 1, 0, 0, nn * dd * (20 + eb),
+        rows_rmsnorm_bwd(c->dxn, c->sx + (long)si * b * d, c->gains + (long)(2 * l) * d, c->srs_a + (long)si * b,
+                         c->dh32, n, d, c->dy, c->dy16.hi, c->dy16.lo, st));
   }
   // ------------------------------------------------------------------- commit
-  CK(rows_commit(c->kown.hi, sq_.ring_k.hi, (long)b * d, (long)k * d, L, pos0, n, k, d, st));
-  CK(rows_commit(c->vown.hi, sq_.ring_v.hi, (long)b * d, (long)k * d, L, pos0, n, k, d, st));
+  const double cb = (double)L * nn * dd * 2 * 2;
+  RUN(K_COMMIT, 1, 0, 0, cb, rows_commit(c->kown.hi, sq_.ring_k.hi, (long)b * d, (long)k * d, L, pos0, n, k, d, st));
+  RUN(K_COMMIT, 1, 0, 0, cb, rows_commit(c->vown.hi, sq_.ring_v.hi, (long)b * d, (long)k * d, L, pos0, n, k, d, st));
   if (sp) {
-    CK(rows_commit(c->kown.lo, sq_.ring_k.lo, (long)b * d, (long)k * d, L, pos0, n, k, d, st));
-    CK(rows_commit(c->vown.lo, sq_.ring_v.lo, (long)b * d, (long)k * d, L, pos0, n, k, d, st));
+    RUN(K_COMMIT, 1, 0, 0, cb,
+        rows_commit(c->kown.lo, sq_.ring_k.lo, (long)b * d, (long)k * d, L, pos0, n, k, d, st));
+    RUN(K_COMMIT, 1, 0, 0, cb,
+        rows_commit(c->vown.lo, sq_.ring_v.lo, (long)b * d, (long)k * d, L, pos0, n, k, d, st));
   }
   sq_.pos = pos0 + n;
   return TTT_OK;
 }
-
 }  // namespace
 
 // ============================================================================ C ABI
@@ -387,6 +493,9 @@ extern "C" int ttt_create(const ttt_config* cfg, void* cuda_stream, ttt_ctx** ou
     s.up16 = palloc(c, S * d * f, ok);
     s.down16 = palloc(c, S * f * d, ok);
   }
+  c->init_up = dalloc<float>(c, S * d * f, ok);
+  c->init_down = dalloc<float>(c, S * f * d, ok);
+  c->acc.resize(K_NCLS);
   c->tok = dalloc<int>(c, (size_t)g.n_seqs * b, ok);
   c->tgt = dalloc<int>(c, b, ok);
   c->next = dalloc<int>(c, g.n_seqs, ok);
@@ -457,6 +566,7 @@ extern "C" void ttt_destroy(ttt_ctx* c) {
   if (c->st) cudaStreamSynchronize(c->st);
   cudaDeviceSynchronize();
   for (void* p : c->allocs) cudaFree(p);
+  for (cudaEvent_t e : c->ev_pool) cudaEventDestroy(e);
   delete c;
 }
 
@@ -503,6 +613,8 @@ extern "C" int ttt_load_weights(ttt_ctx* c, const float* blob, size_t n_floats) 
         CK(rows_convert(down, f, (int)d, d, wd.hi, wd.lo, d, st));
       } else {
         const long si = l - (L - S);
+        CK(cudaMemcpyAsync(c->init_up + si * d * f, up, (size_t)d * f * 4, cudaMemcpyDeviceToDevice, st));
+        CK(cudaMemcpyAsync(c->init_down + si * f * d, down, (size_t)f * d * 4, cudaMemcpyDeviceToDevice, st));
         for (auto& s : c->seqs) {
           CK(cudaMemcpyAsync(s.up32 + si * d * f, up, (size_t)d * f * 4, cudaMemcpyDeviceToDevice, st));
           CK(cudaMemcpyAsync(s.down32 + si * f * d, down, (size_t)f * d * 4, cudaMemcpyDeviceToDevice, st));
@@ -619,5 +731,75 @@ extern "C" int ttt_get_fast_weights(ttt_ctx* c, int32_t seq, int32_t sl, float* 
   if (e == cudaSuccess && w_down)
     e = cudaMemcpy(w_down, c->seqs[seq].down32 + sl * f * d, (size_t)f * d * 4, cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return fail(c, TTT_ERR_CUDA, cudaGetErrorString(e));
+  return TTT_OK;
+}
+
+extern "C" int ttt_reset(ttt_ctx* c) {
+  if (!c) return TTT_ERR_ARG;
+  if (!c->loaded) return fail(c, TTT_ERR_STATE, "weights not loaded");
+  const long L = c->L, S = c->S, d = c->d, f = c->f, k = c->k;
+  cudaStream_t st = c->st;
+  for (auto& s : c->seqs) {
+    s.pos = 0;
+    CK(cudaMemcpyAsync(s.up32, c->init_up, (size_t)S * d * f * 4, cudaMemcpyDeviceToDevice, st));
+    CK(cudaMemcpyAsync(s.down32, c->init_down, (size_t)S * f * d * 4, cudaMemcpyDeviceToDevice, st));
+    CK(rows_convert(c->init_up, S * d, (int)f, f, s.up16.hi, s.up16.lo, f, st));
+    CK(rows_convert(c->init_down, S * f, (int)d, d, s.down16.hi, s.down16.lo, d, st));
+    const size_t rb = (size_t)L * k * d * sizeof(bf16);
+    CK(cudaMemsetAsync(s.ring_k.hi, 0, rb, st));
+    CK(cudaMemsetAsync(s.ring_v.hi, 0, rb, st));
+    if (c->split) {
+      CK(cudaMemsetAsync(s.ring_k.lo, 0, rb, st));
+      CK(cudaMemsetAsync(s.ring_v.lo, 0, rb, st));
+    }
+  }
+  c->launches += 2 * (long)c->seqs.size();
+  return TTT_OK;
+}
+
+extern "C" int64_t ttt_launch_count(const ttt_ctx* c) { return c ? c->launches : -1; }
+
+extern "C" int ttt_profile(ttt_ctx* c, int enable) {
+  if (!c) return TTT_ERR_ARG;
+  if (cudaStreamSynchronize(c->st) != cudaSuccess) return fail(c, TTT_ERR_CUDA, "stream synchronize");
+  c->recs.clear();
+  c->ev_used = 0;
+  for (auto& a : c->acc) a = ttt_ctx::ProfAcc();
+  c->prof_on = enable != 0;
+  return TTT_OK;
+}
+
+extern "C" int ttt_profile_read(ttt_ctx* c, ttt_kernel_stat* out, int max_out, int* n_out) {
+  if (!c || !n_out || (max_out > 0 && !out)) return TTT_ERR_ARG;
+  cudaError_t e = cudaStreamSynchronize(c->st);
+  if (e != cudaSuccess) return fail(c, TTT_ERR_CUDA, cudaGetErrorString(e));
+  for (const auto& r : c->recs) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess) return fail(c, TTT_ERR_CUDA, "event elapsed time");
+    auto& a = c->acc[r.cls];
+    a.launches += r.nkern;
+    a.ms += ms;
+    a.alg += r.alg;
+    a.exec += r.exec;
+    a.bytes += r.bytes;
+  }
+  c->recs.clear();
+  c->ev_used = 0;
+  int n = 0;
+  for (int i = 0; i < K_NCLS; ++i) {
+    if (c->acc[i].launches == 0) continue;
+    if (n < max_out) {
+      ttt_kernel_stat& o = out[n];
+      std::memset(&o, 0, sizeof(o));
+      std::snprintf(o.name, sizeof(o.name), "%s", kClsName[i]);
+      o.launches = c->acc[i].launches;
+      o.ms = c->acc[i].ms;
+      o.alg_flops = c->acc[i].alg;
+      o.exec_flops = c->acc[i].exec;
+      o.bytes = c->acc[i].bytes;
+    }
+    ++n;
+  }
+  *n_out = n;
   return TTT_OK;
 }

@@ -12,8 +12,9 @@ through a seeded permutation, then 32-token spans copied to random later
 offsets (T // 128 copies) so that the stream contains exact repeats the fast
 weights can learn.
 
-Weights: every matrix N(0, 0.02) drawn in float64 from ``default_rng(seed)``
-in blob order and stored as float32; RMSNorm gains are 1 and are not drawn.
+Weights: every matrix N(0, 0.02), drawn as float32 standard normals from
+``default_rng(seed)`` in blob order and scaled in float32; RMSNorm gains are 1
+and are not drawn.
 """
 from __future__ import annotations
 
@@ -95,7 +96,7 @@ def blob_size(shape: Shape) -> int:
 
 
 def weight_blob(shape: Shape, seed: int = 0, std: float = 0.02) -> np.ndarray:
-    """fp32 weight blob: N(0, std) matrices (drawn in fp64), unit gains."""
+    """fp32 weight blob: N(0, std) matrices, unit gains."""
     rng = np.random.default_rng(seed)
     blob = np.empty(blob_size(shape), dtype=np.float32)
     off = 0
@@ -104,10 +105,9 @@ def weight_blob(shape: Shape, seed: int = 0, std: float = 0.02) -> np.ndarray:
         if is_gain:
             blob[off:off + n] = 1.0
         else:
-            step = 1 << 24              # bounded fp64 temporaries
-            for i in range(0, n, step):
-                m = min(step, n - i)
-                blob[off + i:off + i + m] = (rng.standard_normal(m) * std).astype(np.float32)
+            seg = blob[off:off + n]
+            rng.standard_normal(n, dtype=np.float32, out=seg)
+            seg *= np.float32(std)
         off += n
     return blob
 
