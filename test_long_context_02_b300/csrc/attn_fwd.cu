@@ -40,9 +40,29 @@ struct FCfg {
   static constexpr int V_OFF = K_OFF + KST * NOP * TILE;
   static constexpr int P_OFF = V_OFF + VST * NOP * TILE;
   static constexpr int BAR_OFF = P_OFF + NP * NOP * PB;
-  static constexpr int SMEM = BAR_OFF + 256 + 1024;
+  static constexpr int XCH_OFF = BAR_OFF + 256;       // row-max / row-sum exchange, [2][2][128] fp32
+  static constexpr int SMEM = XCH_OFF + 2048;          // dynamic smem must start 1024-aligned (checked)
   static_assert(SMEM <= 232448, "attention forward exceeds shared memory");
 };
+
+constexpr int kFwdThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 softmax (two per query row)
+
+// Load N consecutive fp32 TMEM columns (N a multiple of 16) into v.
+template <int N>
+TTT_DEV void tmem_ldn(uint32_t a, float* v) {
+  if constexpr (N >= 32) {
+    float t[32];
+    tmem_ld32(a, t);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = t[i];
+    tmem_ldn<N - 32>(a + 32, v + 32);
+  } else if constexpr (N == 16) {
+    float t[16];
+    tmem_ld16(a, t);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = t[i];
+  }
+}
 
 TTT_DEV bool wait_drain(uint64_t* bar, uint32_t parity, int* err) {
   const uint64_t t0 = globaltimer();
@@ -91,7 +111,7 @@ TTT_DEV TileRange tiles_for(const AttnArgs& a, int qt) {
 }
 
 template <int DH, bool SPLIT>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kFwdThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap tQl,
                     const __grid_constant__ CUtensorMap tKr, const __grid_constant__ CUtensorMap tKrl,
                     const __grid_constant__ CUtensorMap tVr, const __grid_constant__ CUtensorMap tVrl,
@@ -99,8 +119,12 @@ __global__ void __launch_bounds__(192, 1)
                     const __grid_constant__ CUtensorMap tVo, const __grid_constant__ CUtensorMap tVol,
                     const AttnArgs a) {
   using C = FCfg<DH, SPLIT>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  constexpr int HO = DH / 2;  // output columns per softmax thread
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if (smem_u32(smem) & 1023u) {  // the swizzled tiles need a 1024-B aligned base; report, do nothing else
+    if (threadIdx.x == 0 && a.err) atomicCAS(a.err, 0, (int)DERR_SMEM_ALIGN);
+    return;
+  }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
   uint64_t* q_full = bars;
   uint64_t* k_full = q_full + 1;
@@ -111,9 +135,11 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* p_full = s_full + 2;
   uint64_t* o_full = p_full + C::NP;
   uint64_t* o_empty = o_full + 2;
-  uint64_t* drain = o_empty + 2;
+  uint64_t* pairbar = o_empty + 2;  // [4]: the two softmax warps of one TMEM lane quadrant
+  uint64_t* drain = pairbar + 4;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* xch = reinterpret_cast<float*>(smem + C::XCH_OFF);  // [parity][half][row]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qt = blockIdx.x, h = blockIdx.y;
@@ -125,8 +151,9 @@ __global__ void __launch_bounds__(192, 1)
     mbar_init(q_full, 1);
     for (int i = 0; i < C::KST; ++i) { mbar_init(&k_full[i], 1); mbar_init(&k_empty[i], 1); }
     for (int i = 0; i < C::VST; ++i) { mbar_init(&v_full[i], 1); mbar_init(&v_empty[i], 1); }
-    for (int i = 0; i < 2; ++i) { mbar_init(&s_full[i], 1); mbar_init(&o_full[i], 1); mbar_init(&o_empty[i], 128); }
-    for (int i = 0; i < C::NP; ++i) mbar_init(&p_full[i], 128);
+    for (int i = 0; i < 2; ++i) { mbar_init(&s_full[i], 1); mbar_init(&o_full[i], 1); mbar_init(&o_empty[i], 256); }
+    for (int i = 0; i < C::NP; ++i) mbar_init(&p_full[i], 256);
+    for (int i = 0; i < 4; ++i) mbar_init(&pairbar[i], 64);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -244,47 +271,48 @@ __global__ void __launch_bounds__(192, 1)
       mma_commit(drain);
       wait_drain(drain, 0, a.err);
     }
-  } else {  // -------------------------------------------------------------- softmax warps
-    const int qd = warp & 3;
-    const int r = qd * 32 + lane;
+  } else {  // --------------------------------------------------- softmax: two threads per query row
+    const int sw = warp - 2;
+    const int hf = sw >> 2;          // which 64 key columns of each tile (and half of the head dim)
+    const int qd = warp & 3;         // TMEM lane quadrant of this warp
+    const int r = qd * 32 + lane;    // query row within the tile
     const long p = a.pos0 + 128L * qt + r;
     const bool rvalid = 128 * qt + r < a.n;
     const float sl2 = a.scale_log2;
     const uint32_t trow = tmem + ((uint32_t)(qd * 32) << 16);
-    float o[DH];
+    float o[HO];
 #pragma unroll
-    for (int i = 0; i < DH; ++i) o[i] = 0.f;
+    for (int i = 0; i < HO; ++i) o[i] = 0.f;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
 
-    auto accumulate = [&](int jp, float alpha) -> bool {  // O <- (O + O_jp) * alpha
+    auto accumulate = [&](int jp, float alpha) -> bool {  // O <- (O + O_jp) * alpha on this thread's columns
       const bool got = mbar_wait(&o_full[jp & 1], (jp >> 1) & 1, abort_flag, a.err, DERR_TIMEOUT_EPILOGUE);
       if (!__all_sync(0xffffffffu, got)) return false;
       tc_fence_after();
-      const uint32_t ob = trow + 256u + (uint32_t)((jp & 1) * C::DP);
+      float v[HO];
+      tmem_ldn<HO>(trow + 256u + (uint32_t)((jp & 1) * C::DP + hf * HO), v);
 #pragma unroll
-      for (int c = 0; c < DH / 32; ++c) {
-        float v[32];
-        tmem_ld32(ob + c * 32, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o[c * 32 + i] = (o[c * 32 + i] + v[i]) * alpha;
-      }
+      for (int i = 0; i < HO; ++i) o[i] = (o[i] + v[i]) * alpha;
       tc_fence_before();
       mbar_arrive(&o_empty[jp & 1]);
       return true;
     };
+    // exchange a per-row value with the partner thread (same row, other half); phase ph
+    auto exchange = [&](float mine, int ph, float& other) -> bool {
+      xch[(ph & 1) * 256 + hf * 128 + r] = mine;
+      mbar_arrive(&pairbar[qd]);
+      const bool got = mbar_wait(&pairbar[qd], ph & 1, abort_flag, a.err, DERR_TIMEOUT_EPILOGUE);
+      if (!__all_sync(0xffffffffu, got)) return false;
+      other = xch[(ph & 1) * 256 + (hf ^ 1) * 128 + r];
+      return true;
+    };
 
-    for (int j = 0; j < J && ok; ++j) {
-      bool own;
+    for (int j = 0; j < J; ++j) {
       long kpos0;
-      if (j < tr.n_ring) {
-        own = false;
-        kpos0 = 128L * (tr.m_lo + j);
-      } else {
-        own = true;
-        kpos0 = a.pos0 + 128L * (j - tr.n_ring);
-      }
-      int c_lo, c_hi;
+      const bool own = j >= tr.n_ring;
+      kpos0 = own ? a.pos0 + 128L * (j - tr.n_ring) : 128L * (tr.m_lo + j);
+      int c_lo, c_hi;  // visible key columns [c_lo, c_hi] of this tile for this row
       if (!rvalid) {
         c_lo = 0;
         c_hi = -1;
@@ -295,28 +323,39 @@ __global__ void __launch_bounds__(192, 1)
         c_lo = (int)max(0L, p - a.window + 1 - kpos0);
         c_hi = (int)min(127L, a.pos0 - 1 - kpos0);
       }
-      const bool full = (c_lo <= 0 && c_hi >= 127);
+      const int b0 = hf * 64;
+      const bool full = __all_sync(0xffffffffu, c_lo <= b0 && c_hi >= b0 + 63);
       const bool got = mbar_wait(&s_full[j & 1], (j >> 1) & 1, abort_flag, a.err, DERR_TIMEOUT_EPILOGUE);
       if (!__all_sync(0xffffffffu, got)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t sb = trow + (uint32_t)((j & 1) * 128);
+      float v[64];
+      {
+        const uint32_t sb = trow + (uint32_t)((j & 1) * 128 + b0);
+        tmem_ldn<64>(sb, v);
+      }
       float mx = -INFINITY;
+      if (full) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float v[32];
-        tmem_ld32(sb + c * 32, v);
+        for (int i = 0; i < 64; ++i) mx = fmaxf(mx, v[i]);
+      } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int col = c * 32 + i;
-          if (full || (col >= c_lo && col <= c_hi)) mx = fmaxf(mx, v[i]);
+        for (int i = 0; i < 64; ++i) {
+          const bool valid = (b0 + i >= c_lo) && (b0 + i <= c_hi);
+          v[i] = valid ? v[i] : -INFINITY;
+          mx = fmaxf(mx, v[i]);
         }
       }
-      const float m_new = fmaxf(m_run, mx * sl2);
+      float mo;
+      if (!exchange(mx, j, mo)) {
+        ok = false;
+        break;
+      }
+      const float m_new = fmaxf(m_run, fmaxf(mx, mo) * sl2);
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = exp2f(m_run - m_use);
+      const float alpha = ex2_approx(m_run - m_use);
       if (C::NP == 1 && j > 0) {
         if (!accumulate(j - 1, alpha)) {
           ok = false;
@@ -324,39 +363,26 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
       const int pb = j % C::NP;
-      uint8_t* pbuf = smem + C::P_OFF + pb * C::NOP * C::PB;
+      uint8_t* pbuf = smem + C::P_OFF + pb * C::NOP * C::PB + hf * 16384 + r * 128;
       float rs = 0.f;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float v[32];
-        tmem_ld32(sb + c * 32, v);
+      for (int u = 0; u < 8; ++u) {  // 8 x 16-B chunks: columns b0 + 8u .. b0 + 8u + 7 (128-B swizzle)
+        uint32_t hw[4], lw[4];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int col = c * 32 + i;
-          const bool valid = full || (col >= c_lo && col <= c_hi);
-          v[i] = valid ? exp2f(v[i] * sl2 - m_use) : 0.f;
-          rs += v[i];
-        }
-        // 4 x 16-B chunks of row r, columns 32c .. 32c+31 (128-B swizzle)
-        const int atom = c >> 1;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int ch = ((c & 1) * 4 + u) ^ (r & 7);
-          uint32_t hw[4], lw[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float x0 = v[u * 8 + 2 * e], x1 = v[u * 8 + 2 * e + 1];
-            __nv_bfloat162 t = __floats2bfloat162_rn(x0, x1);
-            hw[e] = *reinterpret_cast<uint32_t*>(&t);
-            if (SPLIT) {
-              float2 f = __bfloat1622float2(t);
-              lw[e] = pack_bf16(x0 - f.x, x1 - f.y);
-            }
+        for (int e = 0; e < 4; ++e) {
+          const float x0 = ex2_approx(fmaf(v[8 * u + 2 * e], sl2, -m_use));
+          const float x1 = ex2_approx(fmaf(v[8 * u + 2 * e + 1], sl2, -m_use));
+          rs += x0 + x1;
+          __nv_bfloat162 t = __floats2bfloat162_rn(x0, x1);
+          hw[e] = *reinterpret_cast<uint32_t*>(&t);
+          if (SPLIT) {
+            float2 f = __bfloat1622float2(t);
+            lw[e] = pack_bf16(x0 - f.x, x1 - f.y);
           }
-          uint8_t* dst = pbuf + atom * 16384 + r * 128 + ch * 16;
-          *reinterpret_cast<uint4*>(dst) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-          if (SPLIT) *reinterpret_cast<uint4*>(dst + C::PB) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
+        uint8_t* dst = pbuf + ((u ^ (r & 7)) * 16);
+        *reinterpret_cast<uint4*>(dst) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        if (SPLIT) *reinterpret_cast<uint4*>(dst + C::PB) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
       }
       fence_proxy_async();
       tc_fence_before();
@@ -370,26 +396,25 @@ __global__ void __launch_bounds__(192, 1)
       }
       m_run = m_new;
     }
-    if (J > 0 && ok) {
-      if (accumulate(J - 1, 1.0f) && rvalid) {
-        const float inv = 1.0f / l_run;
-        const long orow = (long)(128 * qt + r) * a.ldo + col0;
+    float l_other = 0.f;
+    if (J > 0 && ok && accumulate(J - 1, 1.0f) && exchange(l_run, J, l_other) && rvalid) {
+      const float inv = 1.0f / (l_run + l_other);
+      const long orow = (long)(128 * qt + r) * a.ldo + col0 + hf * HO;
 #pragma unroll
-        for (int c = 0; c < DH / 8; ++c) {
-          uint32_t hw[4], lw[4];
+      for (int c = 0; c < HO / 8; ++c) {
+        uint32_t hw[4], lw[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float x0 = o[c * 8 + 2 * e] * inv, x1 = o[c * 8 + 2 * e + 1] * inv;
-            __nv_bfloat162 t = __floats2bfloat162_rn(x0, x1);
-            hw[e] = *reinterpret_cast<uint32_t*>(&t);
-            float2 f = __bfloat1622float2(t);
-            lw[e] = pack_bf16(x0 - f.x, x1 - f.y);
-          }
-          *reinterpret_cast<uint4*>(a.o_hi + orow + c * 8) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-          if (a.o_lo) *reinterpret_cast<uint4*>(a.o_lo + orow + c * 8) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        for (int e = 0; e < 4; ++e) {
+          const float x0 = o[c * 8 + 2 * e] * inv, x1 = o[c * 8 + 2 * e + 1] * inv;
+          __nv_bfloat162 t = __floats2bfloat162_rn(x0, x1);
+          hw[e] = *reinterpret_cast<uint32_t*>(&t);
+          float2 f = __bfloat1622float2(t);
+          lw[e] = pack_bf16(x0 - f.x, x1 - f.y);
         }
-        if (a.lse) a.lse[(long)h * a.n + 128 * qt + r] = m_run + log2f(l_run);
+        *reinterpret_cast<uint4*>(a.o_hi + orow + c * 8) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        if (a.o_lo) *reinterpret_cast<uint4*>(a.o_lo + orow + c * 8) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
       }
+      if (a.lse && hf == 0) a.lse[(long)h * a.n + 128 * qt + r] = m_run + log2f(l_run + l_other);
     }
   }
 
@@ -412,7 +437,7 @@ int launch_fwd(const AttnMaps& m, const AttnArgs& a, cudaStream_t st) {
     attr = true;
   }
   dim3 grid((a.n + 127) / 128, a.H);
-  kern<<<grid, 192, C::SMEM, st>>>(m.q, m.ql, m.kr, m.krl, m.vr, m.vrl, m.ko, m.kol, m.vo, m.vol, a);
+  kern<<<grid, kFwdThreads, C::SMEM, st>>>(m.q, m.ql, m.kr, m.krl, m.vr, m.vrl, m.ko, m.kol, m.vo, m.vol, a);
   return (int)cudaGetLastError();
 }
 

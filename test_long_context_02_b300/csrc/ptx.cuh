@@ -20,6 +20,7 @@ enum DevErr : int {
   DERR_TIMEOUT_EPILOGUE = 3,
   DERR_BAD_TOKEN = 4,
   DERR_TIMEOUT_DRAIN = 5,
+  DERR_SMEM_ALIGN = 6,
 };
 
 constexpr unsigned long long kWaitLimitNs = 4000000000ull;   // 4 s
@@ -139,6 +140,29 @@ TTT_DEV void tmem_ld32(uint32_t taddr, float (&v)[32]) {
       : "memory");
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 32 lanes x 16 consecutive fp32 columns (same conventions as tmem_ld32).
+TTT_DEV void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 2^x with the documented ex2.approx.ftz.f32 instruction (relative error ~2^-22;
+// -inf -> 0).  Used for softmax probabilities.
+TTT_DEV float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format: version 1
