@@ -75,14 +75,13 @@ TTT_DEV uint64_t kmajor_desc(uint32_t base, int kk) {
 }
 TTT_DEV uint64_t mnmajor_desc(uint32_t base, int kk) { return sdesc_sw128(base + kk * 2048, 16384, 1024); }
 
-// Write 32 fp32 values as bf16 (and remainders) into row r, columns 32c..32c+31 of a
-// 128 x 128 K-major swizzled tile (two 16 KB atoms of 64 columns).
+// Write 32 fp32 values (columns 32c..32c+31 of one 64-column atom) as bf16 (and
+// remainders) into a 128-B swizzled row; rowp = atom base + r * 128.
 template <bool SPLIT>
-TTT_DEV void put_row32(uint8_t* buf, int r, int c, const float (&v)[32], int lo_off) {
-  const int atom = c >> 1;
+TTT_DEV void put_half_row32(uint8_t* rowp, int r, int c, const float (&v)[32], int lo_off) {
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
-    const int ch = ((c & 1) * 4 + u) ^ (r & 7);
+    const int ch = (c * 4 + u) ^ (r & 7);
     uint32_t hw[4], lw[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -94,11 +93,29 @@ TTT_DEV void put_row32(uint8_t* buf, int r, int c, const float (&v)[32], int lo_
         lw[e] = pack_bf16(x0 - f.x, x1 - f.y);
       }
     }
-    uint8_t* dst = buf + atom * 16384 + r * 128 + ch * 16;
+    uint8_t* dst = rowp + ch * 16;
     *reinterpret_cast<uint4*>(dst) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
     if (SPLIT) *reinterpret_cast<uint4*>(dst + lo_off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
   }
 }
+
+template <int N>
+TTT_DEV void tmem_ldn(uint32_t a, float* v) {
+  if constexpr (N >= 32) {
+    float t[32];
+    tmem_ld32(a, t);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = t[i];
+    tmem_ldn<N - 32>(a + 32, v + 32);
+  } else if constexpr (N == 16) {
+    float t[16];
+    tmem_ld16(a, t);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = t[i];
+  }
+}
+
+constexpr int kBwdThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 two threads per row
 
 struct TileRange {
   int n_ring, m_lo, J;
@@ -121,7 +138,7 @@ TTT_DEV TileRange tiles_for(const AttnArgs& a, int qt) {
 
 // ================================================================ dQ kernel
 template <int DH, bool SPLIT>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     attn_dq_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap tQl,
                    const __grid_constant__ CUtensorMap tDO, const __grid_constant__ CUtensorMap tDOl,
                    const __grid_constant__ CUtensorMap tKr, const __grid_constant__ CUtensorMap tKrl,
@@ -159,7 +176,7 @@ __global__ void __launch_bounds__(192, 1)
     mbar_init(v_empty, 1);
     mbar_init(&s_full[0], 1);
     mbar_init(&s_full[1], 1);
-    for (int i = 0; i < C::NDS; ++i) { mbar_init(&ds_full[i], 128); mbar_init(&ds_empty[i], 1); }
+    for (int i = 0; i < C::NDS; ++i) { mbar_init(&ds_full[i], 256); mbar_init(&ds_empty[i], 1); }
     mbar_init(dq_full, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -271,44 +288,44 @@ __global__ void __launch_bounds__(192, 1)
       mma_commit(drain);
       wait_drain(drain, 0, g.err);
     }
-  } else {  // ------------------------------------------------------------ softmax
-    const int qd = warp & 3, r = qd * 32 + lane;
+  } else {  // ------------------------------------------------- softmax: two threads per query row
+    const int hf = (warp - 2) >> 2, qd = warp & 3, r = qd * 32 + lane;
     const long p = g.pos0 + 128L * qt + r;
     const bool rvalid = 128 * qt + r < g.n;
     const float sl2 = g.scale_log2;
     const uint32_t trow = tmem + ((uint32_t)(qd * 32) << 16);
     const float lse2 = rvalid ? a.lse[(long)h * g.n + 128 * qt + r] : 0.f;
     const float Dr = rvalid ? a.D[(long)h * g.n + 128 * qt + r] : 0.f;
+    const int b0 = hf * 64;
     bool ok = true;
     for (int j = 0; j < J; ++j) {
-      long kpos0;
-      bool own = j >= tr.n_ring;
-      kpos0 = own ? g.pos0 + 128L * (j - tr.n_ring) : 128L * (tr.m_lo + j);
+      const bool own = j >= tr.n_ring;
+      const long kpos0 = own ? g.pos0 + 128L * (j - tr.n_ring) : 128L * (tr.m_lo + j);
       int c_lo, c_hi;
       if (!rvalid) { c_lo = 0; c_hi = -1; }
       else if (own) { c_lo = 0; c_hi = (int)min(127L, p - kpos0); }
       else { c_lo = (int)max(0L, p - g.window + 1 - kpos0); c_hi = (int)min(127L, g.pos0 - 1 - kpos0); }
-      const bool full = (c_lo <= 0 && c_hi >= 127);
+      const bool full = __all_sync(0xffffffffu, c_lo <= b0 && c_hi >= b0 + 63);
       bool got = mbar_wait(&s_full[j & 1], (j >> 1) & 1, abort_flag, g.err, DERR_TIMEOUT_EPILOGUE);
       const int b = j % C::NDS, u = j / C::NDS;
       if (got && u >= 1) got = mbar_wait(&ds_empty[b], (u - 1) & 1, abort_flag, g.err, DERR_TIMEOUT_EPILOGUE);
       if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
       tc_fence_after();
-      uint8_t* dsbuf = smem + C::DS_OFF + b * C::NOP * C::PB;
-      const uint32_t sb = trow + (uint32_t)((j & 1) * 128);
+      uint8_t* dsrow = smem + C::DS_OFF + b * C::NOP * C::PB + hf * 16384 + r * 128;
+      const uint32_t sb = trow + (uint32_t)((j & 1) * 128 + b0);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float s[32], dp[32];
-        tmem_ld32(sb + c * 32, s);
-        tmem_ld32(trow + T_DP + c * 32, dp);
+      for (int c = 0; c < 2; ++c) {
+        float sv[32], dp[32];
+        tmem_ld32(sb + c * 32, sv);
+        tmem_ld32(trow + T_DP + b0 + c * 32, dp);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const int col = c * 32 + i;
-          const bool valid = full || (col >= c_lo && col <= c_hi);
-          const float pr = valid ? exp2f(s[i] * sl2 - lse2) : 0.f;
-          s[i] = pr * (dp[i] - Dr);
+          const int col = b0 + c * 32 + i;
+          float pr = ex2_approx(fmaf(sv[i], sl2, -lse2));
+          if (!full) pr = (col >= c_lo && col <= c_hi) ? pr : 0.f;
+          sv[i] = pr * (dp[i] - Dr);
         }
-        put_row32<SPLIT>(dsbuf, r, c, s, C::PB);
+        put_half_row32<SPLIT>(dsrow, r, c, sv, C::PB);
       }
       fence_proxy_async();
       tc_fence_before();
@@ -317,17 +334,15 @@ __global__ void __launch_bounds__(192, 1)
     bool got = ok && mbar_wait(dq_full, 0, abort_flag, g.err, DERR_TIMEOUT_EPILOGUE);
     if (__all_sync(0xffffffffu, got)) {
       tc_fence_after();
-      const float sc = a.scale;
+      constexpr int HO = DH / 2;
+      float v[HO];
+      tmem_ldn<HO>(trow + T_DQ + hf * HO, v);
+      if (rvalid) {
+        const float sc = a.scale;
+        float4* dst = reinterpret_cast<float4*>(a.dq + (long)(128 * qt + r) * a.ldg + col0 + hf * HO);
 #pragma unroll
-      for (int c = 0; c < DH / 32; ++c) {
-        float v[32];
-        tmem_ld32(trow + T_DQ + c * 32, v);
-        if (rvalid) {
-          float4* dst = reinterpret_cast<float4*>(a.dq + (long)(128 * qt + r) * a.ldg + col0 + c * 32);
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            dst[e] = make_float4(v[4 * e] * sc, v[4 * e + 1] * sc, v[4 * e + 2] * sc, v[4 * e + 3] * sc);
-        }
+        for (int e = 0; e < HO / 4; ++e)
+          dst[e] = make_float4(v[4 * e] * sc, v[4 * e + 1] * sc, v[4 * e + 2] * sc, v[4 * e + 3] * sc);
       }
     }
   }
@@ -341,7 +356,7 @@ __global__ void __launch_bounds__(192, 1)
 
 // ============================================================ dK / dV kernel
 template <int DH, bool SPLIT>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     attn_dkv_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap tQl,
                     const __grid_constant__ CUtensorMap tDO, const __grid_constant__ CUtensorMap tDOl,
                     const __grid_constant__ CUtensorMap tKo, const __grid_constant__ CUtensorMap tKol,
@@ -375,9 +390,9 @@ __global__ void __launch_bounds__(192, 1)
     mbar_init(qd_full, 1);
     mbar_init(qd_empty, 1);
     mbar_init(s_full, 1);
-    mbar_init(p_full, 128);
+    mbar_init(p_full, 256);
     mbar_init(p_free, 1);
-    mbar_init(ds_full, 128);
+    mbar_init(ds_full, 256);
     mbar_init(buf_free, 1);
     mbar_init(acc_full, 1);
     mbar_init(drain, 1);
@@ -468,13 +483,14 @@ __global__ void __launch_bounds__(192, 1)
       mma_commit(drain);
       wait_drain(drain, 0, g.err);
     }
-  } else {  // ------------------------------------------------------------ softmax (one key row each)
-    const int qd = warp & 3, r = qd * 32 + lane;
+  } else {  // --------------------------------------- softmax: two threads per key row (64 queries each)
+    const int hf = (warp - 2) >> 2, qd = warp & 3, r = qd * 32 + lane;
     const int krow = 128 * kt + r;
     const bool kvalid = krow < g.n;
     const float sl2 = g.scale_log2;
     const uint32_t trow = tmem + ((uint32_t)(qd * 32) << 16);
-    uint8_t* pbuf = smem + C::X_P;
+    const int b0 = hf * 64;
+    uint8_t* prow = smem + C::X_P + hf * 16384 + r * 128;
     bool ok = true;
     for (int i = 0; i < I; ++i) {
       const int q0 = 128 * (kt + i);
@@ -484,23 +500,24 @@ __global__ void __launch_bounds__(192, 1)
       const float* sd = a.D + (long)h * g.n + q0;
       const int clast = g.n - 1 - q0;  // columns beyond it are masked and read a clamped index
       // query column c is valid iff q0 + c < n and key position <= query position
-      const int c_lo = kvalid ? krow - q0 : 128;        // first column with q >= key
+      const int c_lo = kvalid ? krow - q0 : 128;
       const int c_hi = min(127, g.n - 1 - q0);
+      const bool full = __all_sync(0xffffffffu, c_lo <= b0 && c_hi >= b0 + 63);
       bool got = mbar_wait(s_full, i & 1, abort_flag, g.err, DERR_TIMEOUT_EPILOGUE);
       if (got && i > 0) got = mbar_wait(buf_free, (i - 1) & 1, abort_flag, g.err, DERR_TIMEOUT_EPILOGUE);
       if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
       tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {  // pass A: P^T
-        float s[32];
-        tmem_ld32(trow + T_S + c * 32, s);
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {  // pass A: P^T
+        float pv[32];
+        tmem_ld32(trow + T_S + b0 + c * 32, pv);
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const int col = c * 32 + e;
-          const bool valid = col >= c_lo && col <= c_hi;
-          s[e] = valid ? exp2f(s[e] * sl2 - sl[min(col, clast)]) : 0.f;
+          const int col = b0 + c * 32 + e;
+          const float pr = ex2_approx(fmaf(pv[e], sl2, -sl[min(col, clast)]));
+          pv[e] = (full || (col >= c_lo && col <= c_hi)) ? pr : 0.f;
         }
-        put_row32<SPLIT>(pbuf, r, c, s, C::PB);
+        put_half_row32<SPLIT>(prow, r, c, pv, C::PB);
       }
       fence_proxy_async();
       tc_fence_before();
@@ -508,20 +525,20 @@ __global__ void __launch_bounds__(192, 1)
       got = mbar_wait(p_free, i & 1, abort_flag, g.err, DERR_TIMEOUT_EPILOGUE);
       if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
       tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {  // pass B: dS^T = P^T (dP^T - D)
-        float s[32], dp[32];
-        tmem_ld32(trow + T_S + c * 32, s);
-        tmem_ld32(trow + T_DP + c * 32, dp);
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {  // pass B: dS^T = P^T (dP^T - D)
+        float dp[32], dv[32];
+        tmem_ld32(trow + T_S + b0 + c * 32, dv);
+        tmem_ld32(trow + T_DP + b0 + c * 32, dp);
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const int col = c * 32 + e;
-          const bool valid = col >= c_lo && col <= c_hi;
+          const int col = b0 + c * 32 + e;
           const int cc = min(col, clast);
-          const float pr = valid ? exp2f(s[e] * sl2 - sl[cc]) : 0.f;
-          s[e] = pr * (dp[e] - sd[cc]);
+          float pr = ex2_approx(fmaf(dv[e], sl2, -sl[cc]));
+          pr = (full || (col >= c_lo && col <= c_hi)) ? pr : 0.f;
+          dv[e] = pr * (dp[e] - sd[cc]);
         }
-        put_row32<SPLIT>(pbuf, r, c, s, C::PB);
+        put_half_row32<SPLIT>(prow, r, c, dv, C::PB);
       }
       fence_proxy_async();
       tc_fence_before();
@@ -530,20 +547,18 @@ __global__ void __launch_bounds__(192, 1)
     bool got = ok && mbar_wait(acc_full, 0, abort_flag, g.err, DERR_TIMEOUT_EPILOGUE);
     if (__all_sync(0xffffffffu, got)) {
       tc_fence_after();
-      const float sc = a.scale;
+      constexpr int HO = DH / 2;
+      float v[HO], w[HO];
+      tmem_ldn<HO>(trow + T_DV + hf * HO, v);
+      tmem_ldn<HO>(trow + T_DK + hf * HO, w);
+      if (kvalid) {
+        const float sc = a.scale;
+        float4* dv = reinterpret_cast<float4*>(a.dv + (long)krow * a.ldg + col0 + hf * HO);
+        float4* dk = reinterpret_cast<float4*>(a.dk + (long)krow * a.ldg + col0 + hf * HO);
 #pragma unroll
-      for (int c = 0; c < DH / 32; ++c) {
-        float v[32], w[32];
-        tmem_ld32(trow + T_DV + c * 32, v);
-        tmem_ld32(trow + T_DK + c * 32, w);
-        if (kvalid) {
-          float4* dv = reinterpret_cast<float4*>(a.dv + (long)krow * a.ldg + col0 + c * 32);
-          float4* dk = reinterpret_cast<float4*>(a.dk + (long)krow * a.ldg + col0 + c * 32);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            dv[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
-            dk[e] = make_float4(w[4 * e] * sc, w[4 * e + 1] * sc, w[4 * e + 2] * sc, w[4 * e + 3] * sc);
-          }
+        for (int e = 0; e < HO / 4; ++e) {
+          dv[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+          dk[e] = make_float4(w[4 * e] * sc, w[4 * e + 1] * sc, w[4 * e + 2] * sc, w[4 * e + 3] * sc);
         }
       }
     }
@@ -571,11 +586,11 @@ int launch_bwd(const AttnBwdMaps& m, const AttnBwdArgs& a, cudaStream_t st, int 
   dim3 grid((a.g.n + 127) / 128, a.g.H);
   const AttnMaps& f = m.f;
   if (which != 2) {
-    kq<<<grid, 192, C::SMEM, st>>>(f.q, f.ql, m.dO, m.dOl, f.kr, f.krl, f.vr, f.vrl, f.ko, f.kol, f.vo, f.vol, a);
+    kq<<<grid, kBwdThreads, C::SMEM, st>>>(f.q, f.ql, m.dO, m.dOl, f.kr, f.krl, f.vr, f.vrl, f.ko, f.kol, f.vo, f.vol, a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return (int)e;
   }
-  if (which != 1) kkv<<<grid, 192, C::XSMEM, st>>>(f.q, f.ql, m.dO, m.dOl, f.ko, f.kol, f.vo, f.vol, a);
+  if (which != 1) kkv<<<grid, kBwdThreads, C::XSMEM, st>>>(f.q, f.ql, m.dO, m.dOl, f.ko, f.kol, f.vo, f.vol, a);
   return (int)cudaGetLastError();
 }
 
