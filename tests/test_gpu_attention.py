@@ -71,14 +71,14 @@ def test_attention_forward_backward(n, H, dh, window, pos0, split):
     doh, dol, dov = to_dev(dO, split)
     o_hi = torch.zeros((n, d), dtype=torch.bfloat16, device=dev)
     o_lo = torch.zeros_like(o_hi) if split else None
-    lse = torch.zeros((H, n), device=dev)
+    lse = torch.zeros((H, n), dtype=torch.float32, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     lo = dict(q=dql, kc=kcl, vc=vcl, ko=kol, vo=vol, o=o_lo, do=dol) if split else None
     T.attn_fwd(n, H, dh, window, pos0, dq_, kch, vch, koh, voh, o_hi, lse, split=split, lo=lo, err=err)
 
-    D = torch.zeros((H, n), device=dev)
+    D = torch.zeros((H, n), dtype=torch.float32, device=dev)
     T.attn_rowdot(n, H, dh, doh, o_hi, D, do_lo=dol, o_lo=o_lo)
-    g = [torch.zeros((n, d), device=dev) for _ in range(3)]
+    g = [torch.zeros((n, d), dtype=torch.float32, device=dev) for _ in range(3)]
     T.attn_bwd(n, H, dh, window, pos0, dq_, kch, vch, koh, voh, doh, lse, D, *g, split=split, lo=lo, err=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0

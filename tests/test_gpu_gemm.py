@@ -65,7 +65,7 @@ def errword():
 @pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 0), (1, 1)])
 def test_gemm_f32_layouts(M, N, K, a_mn, b_mn):
     a, b, Aq, Bq = operands(M, N, K, a_mn, b_mn)
-    out = torch.full((M, N + (-N) % 8), float("nan"), device=dev)
+    out = torch.full((M, N + (-N) % 8), float("nan"), dtype=torch.float32, device=dev)
     err = errword()
     T.gemm(T.EPI_F32, M, N, K, a, b, a_mn=a_mn, b_mn=b_mn, out32=out, ldo32=out.shape[1], err=err)
     torch.cuda.synchronize()
@@ -82,7 +82,7 @@ def test_gemm_split_mode_fp32_accuracy(a_mn, b_mn):
     B = RNG.standard_normal((N, K))
     ah, al = split(A.T if a_mn else A)
     bh, bl = split(B.T if b_mn else B)
-    out = torch.zeros((M, N), device=dev)
+    out = torch.zeros((M, N), dtype=torch.float32, device=dev)
     err = errword()
     T.gemm(T.EPI_F32, M, N, K, ah, bh, a_lo=al, b_lo=bl, a_mn=a_mn, b_mn=b_mn, split=True,
            out32=out, ldo32=N, err=err)
@@ -107,7 +107,7 @@ def test_gemm_epilogues():
     x0 = x.cpu().numpy().astype(np.float64)
     T.gemm(T.EPI_RESID, M, N, K, a, b, b_mn=1, out32=x, ldo32=N, resid=x, ldr=N, err=err)
     # GELU
-    pre = torch.zeros((M, N), device=dev)
+    pre = torch.zeros((M, N), dtype=torch.float32, device=dev)
     gh = torch.zeros((M, N), dtype=torch.bfloat16, device=dev)
     gl = torch.zeros_like(gh)
     T.gemm(T.EPI_GELU, M, N, K, a, b, b_mn=1, out32=pre, ldo32=N, out_hi=gh, out_lo=gl, ldo=N, err=err)
@@ -145,8 +145,8 @@ def test_gemm_cross_entropy_epilogues(N):
     tg = torch.tensor(tgt, device=dev)
     bn = 128 if N <= 128 else 256
     ntiles = max(1, -(-N // 256))
-    part = torch.zeros((ntiles + 4) * M * 2, device=dev)
-    zt = torch.zeros(M, device=dev)
+    part = torch.zeros((ntiles + 4) * M * 2, dtype=torch.float32, device=dev)
+    zt = torch.zeros(M, dtype=torch.float32, device=dev)
     err = errword()
     T.gemm(T.EPI_CE_FWD, M, N, K, a, b, b_mn=1, tgt=tg, part=part, zt=zt, err=err)
     torch.cuda.synchronize()

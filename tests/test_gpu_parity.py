@@ -110,7 +110,7 @@ def test_bad_token_rejected_and_state_errors():
     # the device path reports a bad id at the next sync
     tok = torch.tensor([1, 2, s.vocab + 5], dtype=torch.int32, device="cuda")
     nxt = torch.tensor([-1], dtype=torch.int32, device="cuda")
-    loss = torch.zeros(1, device="cuda")
+    loss = torch.zeros(1, dtype=torch.float32, device="cuda")
     m.prefill_chunk_dev(tok, 3, nxt, loss)
     with pytest.raises(T.TTTError) as e:
         m.sync()

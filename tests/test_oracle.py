@@ -19,8 +19,17 @@ import torch.nn.functional as F
 from oracle import ttt_oracle as O
 from ttt_inputs import SHAPES, sequence_tokens, weight_blob
 
-torch.set_default_dtype(torch.float64)
 RNG = np.random.default_rng(1234)
+
+
+@pytest.fixture(autouse=True)
+def _float64_default():
+    """torch routines used as pins run in float64; the global default is restored
+    afterwards so that tests collected later (GPU buffers) keep float32."""
+    old = torch.get_default_dtype()
+    torch.set_default_dtype(torch.float64)
+    yield
+    torch.set_default_dtype(old)
 
 
 def tiny_cfg(**kw):
