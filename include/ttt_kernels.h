@@ -101,6 +101,42 @@ TTT_API int ttt_k_attn_bwd(int n, int H, int dh, int window, int64_t pos0, int s
 TTT_API int ttt_k_attn_rowdot(int n, int H, int dh, const void* do_hi, const void* do_lo, const void* o_hi,
                               const void* o_lo, float* D, void* stream);
 
+/*
+ * LM-head cross-entropy statistics WITHOUT ANY DEVICE ALLOCATION.  The paper
+ * has no counterpart: this entry point exists for callers that cannot call
+ * cudaMalloc, for example a process whose device memory is owned up front by
+ * another allocator, or a latency-bound caller that cannot take cudaMalloc's
+ * implicit device synchronisation.  It computes what ttt_k_gemm with
+ * TTT_EPI_CE_FWD followed by the per-row combine computes, for bf16 operands:
+ *   z = x . W_lm          x    [M][ldx] bf16 (K-major, K used columns)
+ *                        W_lm [K][ldw] bf16 (row-major, V used columns)
+ *   lse[r]  = log sum_c exp(z[r][c])                        (natural log)
+ *   loss[r] = tgt[r] >= 0 ? lse[r] - z[r][tgt[r]] : 0        tgt[r] in {-1} U [0, V)
+ * x, W_lm, tgt, lse and loss are caller-owned DEVICE memory; err is an
+ * optional device int that a kernel sets if one of its bounded waits expires.
+ *
+ * Scratch: the partial (max, sum) pairs of every (row, vocab tile) and the
+ * target logits live in one file-scope __device__ array of
+ * TTT_CE_STATIC_SCRATCH_ENTRIES float2 (4 MiB), held by every GPU that loads
+ * the library until the process exits.  Every scratch element a call reads is
+ * written earlier in the same call, so nothing needs clearing between calls.
+ * All calls share that one array: calls whose work overlaps on the GPU (other
+ * streams, other host threads) race and give wrong results; serialise them.
+ * Limit: ceil(V / 128) * M + ceil(M / 2) <= TTT_CE_STATIC_SCRATCH_ENTRIES
+ * (e.g. M = 1024 rows with V up to 65,408); larger sizes return
+ * TTT_ERR_SCRATCH before anything is enqueued.
+ * The first call on a device looks up the array's device address with
+ * cudaGetSymbolAddress (once per device, with that device current); make that
+ * first call before any stream capture.  Returns 0, TTT_ERR_ARG (null
+ * pointer, size < 1, pitch < width or not a multiple of 8), TTT_ERR_SCRATCH,
+ * or TTT_ERR_CUDA (symbol lookup or launch failure).
+ */
+#define TTT_CE_STATIC_SCRATCH_ENTRIES 524288
+#define TTT_ERR_SCRATCH (-7)     /* the call needs more static scratch than the library holds */
+TTT_API int ttt_k_lmhead_ce_static(int M, int K, int V, const void* x, int64_t ldx, const void* w_lm,
+                                   int64_t ldw, const int32_t* tgt, float* lse, float* loss, int32_t* err,
+                                   void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -21,9 +21,10 @@ if not os.path.exists(LIB_PATH):
 lib = ctypes.CDLL(LIB_PATH)
 
 TTT_OK, TTT_ERR_ARG, TTT_ERR_UNSUPPORTED, TTT_ERR_STATE = 0, -1, -2, -3
-TTT_ERR_OOM, TTT_ERR_CUDA, TTT_ERR_DEVICE = -4, -5, -6
+TTT_ERR_OOM, TTT_ERR_CUDA, TTT_ERR_DEVICE, TTT_ERR_SCRATCH = -4, -5, -6, -7
 ERR_NAMES = {0: "OK", -1: "TTT_ERR_ARG", -2: "TTT_ERR_UNSUPPORTED", -3: "TTT_ERR_STATE",
-             -4: "TTT_ERR_OOM", -5: "TTT_ERR_CUDA", -6: "TTT_ERR_DEVICE"}
+             -4: "TTT_ERR_OOM", -5: "TTT_ERR_CUDA", -6: "TTT_ERR_DEVICE", -7: "TTT_ERR_SCRATCH"}
+CE_STATIC_SCRATCH_ENTRIES = 524288
 
 EPI_F32, EPI_OPND, EPI_RESID, EPI_GELU, EPI_GELU_BWD, EPI_SGD, EPI_CE_FWD, EPI_CE_BWD = range(8)
 
@@ -107,6 +108,11 @@ ttt_k_attn_bwd = _sig("ttt_k_attn_bwd", ctypes.c_int, ctypes.c_int, ctypes.c_int
 ttt_k_attn_rowdot = _sig("ttt_k_attn_rowdot", ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                          _vp, _vp, _vp, _vp, _vp, _vp)
 
+# No-allocation variant of the LM-head cross-entropy statistics (scratch in a
+# static device array of the library; see include/ttt_kernels.h).
+ttt_k_lmhead_ce_static = _sig("ttt_k_lmhead_ce_static", ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                              _vp, _i64, _vp, _i64, _vp, _vp, _vp, _vp, _vp)
+
 ttt_create = _sig("ttt_create", ctypes.c_int, ctypes.POINTER(ttt_config), _vp, ctypes.POINTER(_vp))
 ttt_load_weights = _sig("ttt_load_weights", ctypes.c_int, _vp, _vp, ctypes.c_size_t)
 ttt_prefill_chunk = _sig("ttt_prefill_chunk", ctypes.c_int, _vp, _vp, _i32, _vp, _vp)
@@ -154,6 +160,14 @@ def attn_bwd(n, H, dh, window, pos0, q, kc, vc, ko, vo, do, lse, D, dq, dk, dv, 
 def attn_rowdot(n, H, dh, do, o, D, *, do_lo=None, o_lo=None, stream=None):
     return check(ttt_k_attn_rowdot(n, H, dh, ptr(do), ptr(do_lo), ptr(o), ptr(o_lo), ptr(D), _stream(stream)),
                  "ttt_k_attn_rowdot")
+
+
+def lmhead_ce_static(M, K, V, x, w_lm, tgt, lse, loss, *, ldx=None, ldw=None, err=None, stream=None):
+    """ttt_k_lmhead_ce_static on torch tensors: lse / loss [M] fp32 from x [M][K] and W_lm [K][V] (bf16)."""
+    ldx = ldx if ldx is not None else x.shape[-1]
+    ldw = ldw if ldw is not None else w_lm.shape[-1]
+    return check(ttt_k_lmhead_ce_static(M, K, V, ptr(x), ldx, ptr(w_lm), ldw, ptr(tgt), ptr(lse), ptr(loss),
+                                        ptr(err), _stream(stream)), "ttt_k_lmhead_ce_static")
 
 
 def make_config(n_layers, d_model, n_heads, d_ff, vocab, window, chunk, rope_theta, eta, n_seqs=1,
