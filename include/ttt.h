@@ -71,7 +71,7 @@ typedef struct {
  * Create a context on the current CUDA device; work goes to `cuda_stream`
  * (cudaStream_t, NULL = default stream).
  * Supported: d_head % 16 == 0 and d_head <= 128 (<= 64 when compute == 0),
- * d_model % 64 == 0, d_ff % 64 == 0, vocab % 8 == 0, window % 128 == 0,
+ * d_model % 64 == 0, d_model <= 4096, d_ff % 64 == 0, vocab % 8 == 0, window % 128 == 0,
  * 1 <= chunk <= window, 1 <= n_trainable <= n_layers.  Otherwise
  * TTT_ERR_UNSUPPORTED (shape) or TTT_ERR_ARG (inconsistent values).
  */
@@ -139,14 +139,16 @@ TTT_API int ttt_reset(ttt_ctx* ctx);
 TTT_API int64_t ttt_launch_count(const ttt_ctx* ctx);
 
 /*
- * Per-kernel-class timing.  ttt_profile(ctx, 1) synchronises, clears the
- * accumulators and starts bracketing every launch with CUDA events on the
- * context stream; ttt_profile(ctx, 0) stops.  ttt_profile_read synchronises,
- * folds the recorded launches into the accumulators and writes up to max_out
- * entries (classes with at least one launch); *n_out = number of such classes.
- * alg_flops counts the multiply-adds the method needs (x2), exec_flops what the
- * kernels execute (masked attention tiles, logit recompute, split-mode triple
- * products), bytes the algorithmic HBM traffic of memory-bound classes.
+ * Per-kernel-class timing.  ttt_profile(ctx, mask) synchronises, clears the
+ * accumulators and starts bracketing with CUDA events (on the context stream)
+ * every launch whose class bit is set in `mask` (bit i = class i, named by
+ * ttt_profile_class_name(i); -1 = every class; 0 = off).  ttt_profile_read
+ * synchronises, folds the recorded launches into the accumulators and writes
+ * up to max_out entries (classes with at least one launch); *n_out = number
+ * of such classes.  alg_flops counts the multiply-adds the method needs (x2),
+ * exec_flops what the kernels execute (masked attention tiles, logit
+ * recompute, split-mode triple products), bytes the algorithmic HBM traffic
+ * of memory-bound classes.
  */
 typedef struct {
   char name[32];
@@ -156,7 +158,9 @@ typedef struct {
   double exec_flops;
   double bytes;
 } ttt_kernel_stat;
-TTT_API int ttt_profile(ttt_ctx* ctx, int enable);
+TTT_API int ttt_profile(ttt_ctx* ctx, int64_t class_mask);
+/* Name of kernel class `cls` (0-based), NULL past the last class. */
+TTT_API const char* ttt_profile_class_name(int cls);
 TTT_API int ttt_profile_read(ttt_ctx* ctx, ttt_kernel_stat* out, int max_out, int* n_out);
 
 /* Current absolute position (tokens consumed) of every sequence. */

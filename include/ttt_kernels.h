@@ -29,7 +29,7 @@ enum {
   TTT_EPI_F32 = 0,      /* out32[r][c] = acc                                          */
   TTT_EPI_OPND = 1,     /* out_hi/lo[r][c] = split(acc)                               */
   TTT_EPI_RESID = 2,    /* out32[r][c] = resid[r][c] + acc   (may alias)              */
-  TTT_EPI_GELU = 3,     /* out32 = acc; out_hi/lo = gelu_tanh(acc)                    */
+  TTT_EPI_GELU = 3,     /* out32 = acc (if out32); out_hi/lo = gelu_tanh(acc)         */
   TTT_EPI_GELU_BWD = 4, /* out_hi/lo = acc * gelu_tanh'(aux[r][c])                    */
   TTT_EPI_SGD = 5,      /* w32 -= eta*acc; w_hi/lo = split(w32)                       */
   TTT_EPI_CE_FWD = 6,   /* part[ntile*M + r] = (max, sum exp(acc - max)) over the
@@ -48,6 +48,9 @@ typedef struct {
   float* w32;  void* w_hi;  void* w_lo;  int64_t ldw;  float eta;
   const int32_t* tgt;  float* part;  float* zt;  const float* lse;  float scale;
   int32_t* err;   /* device int, set non-zero if a bounded wait in the kernel expired */
+  int32_t allow_ksplit; /* F32 / RESID only: non-zero lets the product be cut into K slices
+                           whose partial sums are added atomically into out32 (cleared,
+                           or loaded with resid, first); the summation order then varies */
 } ttt_gemm_epilogue;
 
 /*

@@ -48,7 +48,7 @@ class ttt_gemm_epilogue(ctypes.Structure):
                 ("resid", _vp), ("ldr", _i64), ("aux", _vp), ("ldaux", _i64),
                 ("w32", _vp), ("w_hi", _vp), ("w_lo", _vp), ("ldw", _i64), ("eta", _f32),
                 ("tgt", _vp), ("part", _vp), ("zt", _vp), ("lse", _vp), ("scale", _f32),
-                ("err", _vp)]
+                ("err", _vp), ("allow_ksplit", _i32)]
 
 
 def _sig(name, restype, *argtypes):
@@ -90,7 +90,7 @@ def gemm(epi, M, N, K, a, b, *, a_lo=None, b_lo=None, lda=None, ldb=None, a_mn=0
     """ttt_k_gemm on torch tensors; epilogue fields by name (tensors or scalars)."""
     e = ttt_gemm_epilogue()
     for k, v in epilogue.items():
-        if k in ("ldo32", "ldo", "ldr", "ldaux", "ldw", "eta", "scale"):
+        if k in ("ldo32", "ldo", "ldr", "ldaux", "ldw", "eta", "scale", "allow_ksplit"):
             setattr(e, k, v)
         else:
             setattr(e, k, ptr(v))
@@ -132,7 +132,19 @@ class ttt_kernel_stat(ctypes.Structure):
                 ("alg_flops", ctypes.c_double), ("exec_flops", ctypes.c_double), ("bytes", ctypes.c_double)]
 
 
-ttt_profile = _sig("ttt_profile", ctypes.c_int, _vp, ctypes.c_int)
+ttt_profile = _sig("ttt_profile", ctypes.c_int, _vp, _i64)
+ttt_profile_class_name = _sig("ttt_profile_class_name", ctypes.c_char_p, ctypes.c_int)
+
+
+def profile_classes():
+    """Names of the kernel classes, in class-id order (bit i of a profile mask)."""
+    out, i = [], 0
+    while True:
+        n = ttt_profile_class_name(i)
+        if n is None:
+            return out
+        out.append(n.decode())
+        i += 1
 ttt_profile_read = _sig("ttt_profile_read", ctypes.c_int, _vp, ctypes.POINTER(ttt_kernel_stat), ctypes.c_int,
                         ctypes.POINTER(ctypes.c_int))
 
@@ -242,8 +254,13 @@ class TTT:
     def launches(self) -> int:
         return int(ttt_launch_count(self._h))
 
-    def profile(self, enable: bool):
-        self._check(ttt_profile(self._h, int(enable)), "ttt_profile")
+    def profile(self, enable=True, classes=None):
+        """Start (enable) or stop event timing; `classes` limits it to those class names."""
+        mask = 0
+        if enable:
+            names = profile_classes()
+            mask = -1 if classes is None else sum(1 << names.index(c) for c in classes)
+        self._check(ttt_profile(self._h, mask), "ttt_profile")
 
     def profile_read(self):
         """{class name: dict(launches, ms, alg_flops, exec_flops, bytes)} since ttt_profile(1)."""

@@ -25,6 +25,7 @@ extern "C" int ttt_k_gemm(int epi, int M, int N, int K, const void* a_hi, const 
   g.w32 = e->w32; g.wh = (bf16*)e->w_hi; g.wl = (bf16*)e->w_lo; g.ldw = (long)e->ldw; g.eta = e->eta;
   g.tgt = e->tgt; g.part = (float2*)e->part; g.zt = e->zt; g.lse = e->lse; g.scale = e->scale;
   g.err = e->err;
+  g.allow_ksplit = e->allow_ksplit != 0;
   Opnd A, B;
   A.hi = (const bf16*)a_hi; A.lo = (const bf16*)a_lo; A.ld = (long)lda; A.mn = a_mn ? 1 : 0;
   B.hi = (const bf16*)b_hi; B.lo = (const bf16*)b_lo; B.ld = (long)ldb; B.mn = b_mn ? 1 : 0;

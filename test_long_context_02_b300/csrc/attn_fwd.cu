@@ -452,13 +452,7 @@ int attn_fwd_run(const AttnMaps& m, const AttnArgs& a, bool split, cudaStream_t 
     }
     return (int)cudaErrorInvalidValue;
   }
-  switch (a.dh) {
-    case 32: return launch_fwd<32, false>(m, a, st);
-    case 64: return launch_fwd<64, false>(m, a, st);
-    case 96: return launch_fwd<96, false>(m, a, st);
-    case 128: return launch_fwd<128, false>(m, a, st);
-  }
-  return (int)cudaErrorInvalidValue;
+  return attn_fwd2_run(m, a, st);  // bf16 operands: the two-tile kernel
 }
 
 }  // namespace ttt

@@ -41,7 +41,7 @@ struct Cfg {
   static constexpr int NOP = SPLIT ? 2 : 1;
   static constexpr int STAGE = NOP * (A_BYTES + B_BYTES);
   static constexpr int STAGES = kSmemBudget / STAGE;
-  static constexpr uint32_t TMEM_COLS = 2 * BN;
+  static constexpr uint32_t TMEM_COLS = 2 * BN <= 256 ? 256 : 512;  // power of two >= 2 accumulators
   static constexpr int SMEM = STAGES * STAGE + 1024 + 256;
 };
 
@@ -109,6 +109,26 @@ TTT_DEV void store_opnd32(bf16* hi, bf16* lo, long base, const float (&v)[32], i
   }
 }
 
+// N (multiple of 8) consecutive values of one row as bf16 (+ remainders), 16-byte stores.
+template <int N>
+TTT_DEV void store_opnd_n(bf16* hi, bf16* lo, long base, const float* v) {
+#pragma unroll
+  for (int u = 0; u < N / 8; ++u) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      __nv_bfloat162 t = __floats2bfloat162_rn(v[8 * u + 2 * e], v[8 * u + 2 * e + 1]);
+      h[e] = *reinterpret_cast<uint32_t*>(&t);
+      if (lo) {
+        float2 f = __bfloat1622float2(t);
+        l[e] = pack_bf16(v[8 * u + 2 * e] - f.x, v[8 * u + 2 * e + 1] - f.y);
+      }
+    }
+    *reinterpret_cast<uint4*>(hi + base + 8 * u) = make_uint4(h[0], h[1], h[2], h[3]);
+    if (lo) *reinterpret_cast<uint4*>(lo + base + 8 * u) = make_uint4(l[0], l[1], l[2], l[3]);
+  }
+}
+
 TTT_DEV void store_f32_32(float* p, const float (&v)[32], int ncols) {
   if (ncols == 32) {
     float4* q = reinterpret_cast<float4*>(p);
@@ -116,6 +136,19 @@ TTT_DEV void store_f32_32(float* p, const float (&v)[32], int ncols) {
     for (int i = 0; i < 8; ++i) q[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
   } else {
     for (int i = 0; i < ncols; ++i) p[i] = v[i];
+  }
+}
+
+// out[i] += v[i] for 32 consecutive fp32 values (vector reductions when the fragment is whole).
+TTT_DEV void red_add_f32_32(float* p, const float (&v)[32], int ncols) {
+  if (ncols == 32) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p + 4 * i), "f"(v[4 * i]), "f"(v[4 * i + 1]),
+                   "f"(v[4 * i + 2]), "f"(v[4 * i + 3])
+                   : "memory");
+  } else {
+    for (int i = 0; i < ncols; ++i) atomicAdd(p + i, v[i]);
   }
 }
 
@@ -132,7 +165,7 @@ TTT_DEV void load_f32_32(const float* p, float (&v)[32], int ncols) {
   }
 }
 
-template <int BN, bool SPLIT, int EPI>
+template <int BN, bool SPLIT, int EPI, int DH>
 __global__ void __launch_bounds__(192, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tAl,
                 const __grid_constant__ CUtensorMap tB, const __grid_constant__ CUtensorMap tBl, const GemmArgs g) {
@@ -150,6 +183,10 @@ __global__ void __launch_bounds__(192, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mt = (g.M + BM - 1) / BM, nt = (g.N + BN - 1) / BN, ntiles = mt * nt;
   const int nk = (g.K + BK - 1) / BK;
+  // work unit u = (output tile u % ntiles, K slice u / ntiles); slices > 1 only for
+  // the F32 / RESID epilogues, which then add their partial sums atomically
+  const int ks = g.ksplit > 1 ? g.ksplit : 1;
+  const int nunits = ntiles * ks;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -186,9 +223,11 @@ __global__ void __launch_bounds__(192, 1)
       bool ok = true;
       uint32_t issued = 0;  // bit s: stage s has a fill in flight or landed
       uint32_t iss_par = 0; // bit s: parity of that fill
-      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+        const int t = u % ntiles, sl = u / ntiles;
         const int m0 = (t % mt) * BM, n0 = (t / mt) * BN;
-        for (int kb = 0; kb < nk; ++kb) {
+        const int kb0 = (int)((long)sl * nk / ks), kb1 = (int)((long)(sl + 1) * nk / ks);
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, g.err, DERR_TIMEOUT_PRODUCER)) {
             ok = false;
             break;
@@ -220,13 +259,15 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t ph = 0;
       int it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++it) {
+      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++it) {
+        const int sl = u / ntiles;
+        const int kb0 = (int)((long)sl * nk / ks), kb1 = (int)((long)(sl + 1) * nk / ks);
         const int buf = it & 1;
         const uint32_t use = (uint32_t)(it >> 1);
         if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag, g.err, DERR_TIMEOUT_MMA)) break;
         tc_fence_after();
         const uint32_t dt = tmem + (uint32_t)(buf * BN);
-        for (int kb = 0; kb < nk; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&full[s], ph, abort_flag, g.err, DERR_TIMEOUT_MMA)) {
             ok = false;
             break;
@@ -237,7 +278,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t da = tile_desc(a, kk, g.a_mn), db = tile_desc(b, kk, g.b_mn);
-            mma_bf16(dt, da, db, idesc, (kb | kk) ? 1u : 0u);
+            mma_bf16(dt, da, db, idesc, (kb > kb0 || kk) ? 1u : 0u);
             if (SPLIT) {
               const uint64_t dal = tile_desc(a + C::A_BYTES + C::B_BYTES, kk, g.a_mn);
               const uint64_t dbl = tile_desc(a + 2 * C::A_BYTES + C::B_BYTES, kk, g.b_mn);
@@ -260,7 +301,8 @@ __global__ void __launch_bounds__(192, 1)
   } else {  // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     int it = 0;
-    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+    for (int u = blockIdx.x; u < nunits; u += gridDim.x, ++it) {
+      const int t = u % ntiles;
       const int buf = it & 1;
       const uint32_t use = (uint32_t)(it >> 1);
       const bool got = mbar_wait(&tfull[buf], use & 1u, abort_flag, g.err, DERR_TIMEOUT_EPILOGUE);
@@ -279,6 +321,44 @@ __global__ void __launch_bounds__(192, 1)
         if (EPI == EPI_CE_BWD && rok) lse_r = g.lse[row];
         if (EPI == EPI_CE_BWD) ce_s = g.scale_dev ? *g.scale_dev : g.scale;
       }
+      if constexpr (EPI == EPI_QKV_ROPE) {
+        // The tile holds BN / DH whole heads of one section (q, k or v) of the
+        // [q | k | v] product; q and k are rotated (rotate-half pairs i, i + DH/2,
+        // angle table row = token row) and all three written as bf16 operands.
+        const int sec = n0 / g.rd;
+        const int scol = n0 - sec * g.rd;
+        bf16* oh = sec == 0 ? g.rq_h : (sec == 1 ? g.rk_h : g.rv_h);
+        bf16* ol = sec == 0 ? g.rq_l : (sec == 1 ? g.rk_l : g.rv_l);
+#pragma unroll 1
+        for (int hh = 0; hh < BN / DH; ++hh) {
+          float v[DH];
+#pragma unroll
+          for (int c = 0; c < DH / 32; ++c) {
+            float t[32];
+            tmem_ld32(taddr + (uint32_t)(hh * DH + c * 32), t);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[32 * c + i] = t[i];
+          }
+          if (!rok) continue;
+          if (sec < 2) {
+            const float4* c4 = reinterpret_cast<const float4*>(g.rcs + (long)row * (DH / 2));
+            const float4* s4 = reinterpret_cast<const float4*>(g.rsn + (long)row * (DH / 2));
+#pragma unroll
+            for (int i4 = 0; i4 < DH / 8; ++i4) {
+              const float4 cc = c4[i4], ss = s4[i4];
+              const float cv[4] = {cc.x, cc.y, cc.z, cc.w}, sv[4] = {ss.x, ss.y, ss.z, ss.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int i = 4 * i4 + e;
+                const float x1 = v[i], x2 = v[i + DH / 2];
+                v[i] = x1 * cv[e] - x2 * sv[e];
+                v[i + DH / 2] = x2 * cv[e] + x1 * sv[e];
+              }
+            }
+          }
+          store_opnd_n<DH>(oh, ol, (long)row * g.rd + scol + hh * DH, v);
+        }
+      } else {
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         float v[32];
@@ -286,7 +366,10 @@ __global__ void __launch_bounds__(192, 1)
         const int c0 = n0 + c * 32;
         const int ncols = min(32, g.N - c0);
         if (!rok || ncols <= 0) continue;
-        if (EPI == EPI_F32) {
+        if ((EPI == EPI_F32 || EPI == EPI_RESID) && ks > 1) {
+          // K slice: add the partial sum (out32 holds 0, or the residual, before the first slice lands)
+          red_add_f32_32(g.out32 + (long)row * g.ldo32 + c0, v, ncols);
+        } else if (EPI == EPI_F32) {
           store_f32_32(g.out32 + (long)row * g.ldo32 + c0, v, ncols);
         } else if (EPI == EPI_OPND) {
           store_opnd32(g.oh, g.ol, (long)row * g.ldo + c0, v, ncols);
@@ -297,7 +380,7 @@ __global__ void __launch_bounds__(192, 1)
           for (int i = 0; i < 32; ++i) r[i] += v[i];
           store_f32_32(g.out32 + (long)row * g.ldo32 + c0, r, ncols);
         } else if (EPI == EPI_GELU) {
-          store_f32_32(g.out32 + (long)row * g.ldo32 + c0, v, ncols);
+          if (g.out32) store_f32_32(g.out32 + (long)row * g.ldo32 + c0, v, ncols);
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = gelu_f(v[i]);
           store_opnd32(g.oh, g.ol, (long)row * g.ldo + c0, v, ncols);
@@ -339,6 +422,7 @@ __global__ void __launch_bounds__(192, 1)
           store_opnd32(g.oh, g.ol, (long)row * g.ldo + c0, v, ncols);
         }
       }
+      }
       if (EPI == EPI_CE_FWD && rok) g.part[(long)ntile * g.M + row] = make_float2(ce_m, ce_s);
       tc_fence_before();
       mbar_arrive(&tempty[buf]);
@@ -360,18 +444,18 @@ bool operand_map(CUtensorMap* m, const bf16* p, const Opnd& o, int rows, int K, 
   return make_map(m, p, (uint64_t)rows, (uint64_t)K, (uint64_t)o.ld, 64u);
 }
 
-template <int BN, bool SPLIT, int EPI>
+template <int BN, bool SPLIT, int EPI, int DH = 0>
 int launch(const CUtensorMap& a, const CUtensorMap& al, const CUtensorMap& b, const CUtensorMap& bl,
            const GemmArgs& g, cudaStream_t st) {
   using C = Cfg<BN, SPLIT>;
-  auto kern = gemm_kernel<BN, SPLIT, EPI>;
+  auto kern = gemm_kernel<BN, SPLIT, EPI, DH>;
   static bool attr_set = false;  // per instantiation
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return (int)e;
     attr_set = true;
   }
-  const int tiles = ((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN);
+  const int tiles = ((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN) * (g.ksplit > 1 ? g.ksplit : 1);
   const int grid = tiles < num_sms() ? tiles : num_sms();
   kern<<<grid, 192, C::SMEM, st>>>(a, al, b, bl, g);
   return (int)cudaGetLastError();
@@ -405,13 +489,96 @@ int pick_bn(int M, int N) {
   return (N <= 128 || c128 < c256) ? 128 : 256;
 }
 
+// Tile width of the fused QKV + RoPE product for head width dh and model width d
+// (whole heads per tile, tiles never straddle the q / k / v sections), 0 if none.
+int qkv_rope_bn(int dh, int d, bool split) {
+  if (split && dh > 64) return 0;
+  const int cand[3] = {256, 192, 128};
+  for (int bn : cand) {
+    if (bn % dh || d % bn) continue;
+    if (bn == 192 && dh != 96) continue;
+    if (dh != 32 && dh != 64 && dh != 96 && dh != 128) continue;
+    return bn;
+  }
+  return 0;
+}
+
+template <bool SPLIT>
+int launch_qkv_rope(int bn, int dh, const CUtensorMap& a, const CUtensorMap& al, const CUtensorMap& b,
+                    const CUtensorMap& bl, const GemmArgs& g, cudaStream_t st) {
+  if (bn == 256 && dh == 32) return launch<256, SPLIT, EPI_QKV_ROPE, 32>(a, al, b, bl, g, st);
+  if (bn == 256 && dh == 64) return launch<256, SPLIT, EPI_QKV_ROPE, 64>(a, al, b, bl, g, st);
+  if (bn == 128 && dh == 32) return launch<128, SPLIT, EPI_QKV_ROPE, 32>(a, al, b, bl, g, st);
+  if (bn == 128 && dh == 64) return launch<128, SPLIT, EPI_QKV_ROPE, 64>(a, al, b, bl, g, st);
+  if constexpr (!SPLIT) {
+    if (bn == 192 && dh == 96) return launch<192, false, EPI_QKV_ROPE, 96>(a, al, b, bl, g, st);
+    if (bn == 256 && dh == 128) return launch<256, false, EPI_QKV_ROPE, 128>(a, al, b, bl, g, st);
+    if (bn == 128 && dh == 128) return launch<128, false, EPI_QKV_ROPE, 128>(a, al, b, bl, g, st);
+  }
+  return (int)cudaErrorInvalidValue;
+}
+
+int gemm_qkv_rope(const Opnd& A, const Opnd& B, GemmArgs g, int dh, bool split, cudaStream_t st) {
+  if (g.M <= 0) return 0;
+  const int bn = qkv_rope_bn(dh, g.rd, split);
+  if (bn == 0 || g.N != 3 * g.rd || !g.rcs || !g.rsn || !g.rq_h || !g.rk_h || !g.rv_h)
+    return (int)cudaErrorInvalidValue;
+  if (split && (!A.lo || !B.lo || !g.rq_l || !g.rk_l || !g.rv_l)) return (int)cudaErrorInvalidValue;
+  g.a_mn = A.mn;
+  g.b_mn = B.mn;
+  CUtensorMap a, al, b, bl;
+  if (!operand_map(&a, A.hi, A, g.M, g.K, BM) || !operand_map(&b, B.hi, B, g.N, g.K, bn))
+    return (int)cudaErrorInvalidValue;
+  al = a;
+  bl = b;
+  if (split && (!operand_map(&al, A.lo, A, g.M, g.K, BM) || !operand_map(&bl, B.lo, B, g.N, g.K, bn)))
+    return (int)cudaErrorInvalidValue;
+  return split ? launch_qkv_rope<true>(bn, dh, a, al, b, bl, g, st) : launch_qkv_rope<false>(bn, dh, a, al, b, bl, g, st);
+}
+
+// Tile width and K slices for an M x N x K product: the fewest (waves x tile width x
+// k-blocks per unit) per SM, preferring the wider tile and fewer slices on ties.
+// Slices only when allowed (F32 / RESID epilogues) and each keeps >= 4 k-blocks.
+void choose_tiling(int M, int N, int K, bool allow_slices, int* bn_out, int* ks_out) {
+  const long sms = num_sms();
+  const long mt = (M + BM - 1) / BM, nk = (K + BK - 1) / BK;
+  long best = -1;
+  for (int bn : {256, 128}) {
+    if (bn == 256 && N <= 128) continue;
+    const long tiles = mt * ((N + bn - 1) / bn);
+    for (int ks = 1; ks <= (allow_slices ? 8 : 1); ++ks) {
+      if (ks > 1 && (tiles >= sms || nk / ks < 4)) break;
+      const long units = tiles * ks;
+      const long cost = ((units + sms - 1) / sms) * bn * ((nk + ks - 1) / ks) + 2 * ks;  // + slice overhead
+      if (best < 0 || cost < best) {
+        best = cost;
+        *bn_out = bn;
+        *ks_out = ks;
+      }
+    }
+  }
+}
+
 int gemm_run(int epi, const Opnd& A, const Opnd& B, GemmArgs g, bool split, cudaStream_t st) {
   if (g.M <= 0 || g.N <= 0 || g.K <= 0) return 0;
-  if (epi < 0 || epi >= EPI_COUNT) return (int)cudaErrorInvalidValue;
+  if (epi < 0 || epi >= EPI_COUNT || epi == EPI_QKV_ROPE) return (int)cudaErrorInvalidValue;
   if (split && (!A.lo || !B.lo)) return (int)cudaErrorInvalidValue;
   g.a_mn = A.mn;
   g.b_mn = B.mn;
-  const int bn = pick_bn(g.M, g.N);
+  int bn = pick_bn(g.M, g.N), ks = 1;
+  if ((epi == EPI_F32 || epi == EPI_RESID) && g.allow_ksplit) choose_tiling(g.M, g.N, g.K, true, &bn, &ks);
+  g.ksplit = ks;
+  if (ks > 1) {  // the slices add into out32: start it at 0 (F32) or at the residual (RESID)
+    cudaError_t e;
+    if (epi == EPI_F32)
+      e = cudaMemset2DAsync(g.out32, (size_t)g.ldo32 * 4, 0, (size_t)g.N * 4, (size_t)g.M, st);
+    else if (g.out32 != g.resid)
+      e = cudaMemcpy2DAsync(g.out32, (size_t)g.ldo32 * 4, g.resid, (size_t)g.ldr * 4, (size_t)g.N * 4, (size_t)g.M,
+                            cudaMemcpyDeviceToDevice, st);
+    else
+      e = cudaSuccess;
+    if (e != cudaSuccess) return (int)e;
+  }
   CUtensorMap a, al, b, bl;
   if (!operand_map(&a, A.hi, A, g.M, g.K, BM) || !operand_map(&b, B.hi, B, g.N, g.K, bn))
     return (int)cudaErrorInvalidValue;

@@ -15,12 +15,13 @@ enum Epi : int {
   EPI_F32 = 0,      // out32 = acc
   EPI_OPND = 1,     // (oh, ol) = split(acc)                 -> next GEMM operand
   EPI_RESID = 2,    // out32 = resid + acc                   (residual stream)
-  EPI_GELU = 3,     // out32 = acc ; (oh, ol) = gelu_tanh(acc)
+  EPI_GELU = 3,     // out32 = acc (skipped when out32 is null) ; (oh, ol) = gelu_tanh(acc)
   EPI_GELU_BWD = 4, // (oh, ol) = acc * gelu_tanh'(aux)
   EPI_SGD = 5,      // w32 -= eta*acc ; (wh, wl) = split(w32)  (fused SGD step)
   EPI_CE_FWD = 6,   // per (row, N-tile): (max, sum exp) of logits; zt[row] = logit of target
   EPI_CE_BWD = 7,   // (oh, ol) = (softmax(acc) - onehot(tgt)) * scale, softmax from lse
-  EPI_COUNT = 8
+  EPI_QKV_ROPE = 8, // [q | k | v] product: RoPE on q, k; q, k, v written as bf16 operands (gemm_qkv_rope)
+  EPI_COUNT = 9
 };
 
 struct GemmArgs {
@@ -34,7 +35,16 @@ struct GemmArgs {
   const int* tgt = nullptr; float2* part = nullptr; float* zt = nullptr; const float* lse = nullptr;
   float scale = 0.f;
   const float* scale_dev = nullptr;  // CE_BWD: device copy of the scale (used when non-null)
+  // QKV_ROPE: outputs [M][rd] (hi, lo) for q, k, v; angle tables [M][dh/2]; rd = section width d
+  bf16 *rq_h = nullptr, *rq_l = nullptr, *rk_h = nullptr, *rk_l = nullptr, *rv_h = nullptr, *rv_l = nullptr;
+  const float *rcs = nullptr, *rsn = nullptr;
+  int rd = 0;
   int* err = nullptr;
+  // F32 / RESID: the product may be cut into K slices whose partial sums are added
+  // atomically into out32 (gemm_run clears it, or copies resid into it, first);
+  // the sum order then varies from run to run.
+  bool allow_ksplit = false;
+  int ksplit = 1;  // set by gemm_run
 };
 
 // One GEMM operand in HBM.  K-major: row-major [rows][ld] holding the K index
@@ -51,5 +61,9 @@ struct Opnd {
 int gemm_run(int epi, const Opnd& A, const Opnd& B, GemmArgs args, bool split, cudaStream_t st);
 int num_sms();
 int pick_bn(int M, int N);   // tile width gemm_run will use for an M x N product
+// [q | k | v] = A.B with RoPE applied to q and k in the epilogue (head width dh);
+// returns cudaErrorInvalidValue when no tile width fits whole heads (qkv_rope_bn == 0).
+int gemm_qkv_rope(const Opnd& A, const Opnd& B, GemmArgs args, int dh, bool split, cudaStream_t st);
+int qkv_rope_bn(int dh, int d, bool split);
 
 }  // namespace ttt

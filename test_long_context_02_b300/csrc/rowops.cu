@@ -92,68 +92,88 @@ __global__ void targets_kernel(const int* __restrict__ tok, int n, const int* __
 }
 
 // y = x * g / sqrt(mean(x^2) + eps) -> bf16 (hi, lo); rstd saved when requested.
-__global__ void rmsnorm_kernel(const float* __restrict__ x, const float* __restrict__ g, float eps, int n, int d,
-                               bf16* __restrict__ yh, bf16* __restrict__ yl, float* __restrict__ rstd) {
+// One warp per row; lane l holds columns l*8 + 256*i (i < NCH) in registers, so
+// the row is read from HBM once and every load of the row is in flight at once.
+template <int NCH>
+__global__ void __launch_bounds__(128) rmsnorm_kernel(const float* __restrict__ x, const float* __restrict__ g,
+                                                      float eps, int n, int d, bf16* __restrict__ yh,
+                                                      bf16* __restrict__ yl, float* __restrict__ rstd) {
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (row >= n) return;
   const float* xr = x + (long)row * d;
+  float v[NCH][8];
   float ss = 0.f;
-  for (int c = lane * 8; c < d; c += 256) {
-    float v[8];
-    load8(xr + c, v);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) ss += v[i] * v[i];
+  for (int i = 0; i < NCH; ++i) {
+    const int c = lane * 8 + 256 * i;
+    if (c < d) {
+      load8(xr + c, v[i]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ss += v[i][e] * v[i][e];
+    }
   }
   ss = warp_sum(ss);
   const float r = 1.0f / sqrtf(ss / (float)d + eps);
   if (rstd && lane == 0) rstd[row] = r;
-  for (int c = lane * 8; c < d; c += 256) {
-    float v[8], gg[8];
-    load8(xr + c, v);
-    load8(g + c, gg);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = v[i] * r * gg[i];
-    store8(yh, yl, (long)row * d + c, v);
+  for (int i = 0; i < NCH; ++i) {
+    const int c = lane * 8 + 256 * i;
+    if (c < d) {
+      float gg[8];
+      load8(g + c, gg);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[i][e] = v[i][e] * r * gg[e];
+      store8(yh, yl, (long)row * d + c, v[i]);
+    }
   }
 }
 
 // out = resid + [r g dy - x r^3/d * sum(dy g x)]  (gradient of RMSNorm w.r.t. its input, gain frozen)
-__global__ void rmsnorm_bwd_kernel(const float* __restrict__ dy, const float* __restrict__ x,
-                                   const float* __restrict__ g, const float* __restrict__ rstd,
-                                   const float* resid, int n, int d, float* out, bf16* __restrict__ oh,
-                                   bf16* __restrict__ ol) {
+// Same register layout as the forward: dy and x of the row are read once.
+template <int NCH>
+__global__ void __launch_bounds__(128) rmsnorm_bwd_kernel(const float* __restrict__ dy, const float* __restrict__ x,
+                                                          const float* __restrict__ g, const float* __restrict__ rstd,
+                                                          const float* resid, int n, int d, float* out,
+                                                          bf16* __restrict__ oh, bf16* __restrict__ ol) {
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (row >= n) return;
   const long base = (long)row * d;
+  float a[NCH][8], b[NCH][8];
   float s = 0.f;
-  for (int c = lane * 8; c < d; c += 256) {
-    float a[8], b[8], gg[8];
-    load8(dy + base + c, a);
-    load8(x + base + c, b);
-    load8(g + c, gg);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) s += a[i] * gg[i] * b[i];
+  for (int i = 0; i < NCH; ++i) {
+    const int c = lane * 8 + 256 * i;
+    if (c < d) {
+      float gg[8];
+      load8(dy + base + c, a[i]);
+      load8(x + base + c, b[i]);
+      load8(g + c, gg);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) s += a[i][e] * gg[e] * b[i][e];
+    }
   }
   s = warp_sum(s);
   const float r = rstd[row];
   const float k = r * r * r * s / (float)d;
-  for (int c = lane * 8; c < d; c += 256) {
-    float a[8], b[8], gg[8], rr[8];
-    load8(dy + base + c, a);
-    load8(x + base + c, b);
-    load8(g + c, gg);
-    if (resid) {
-      load8(resid + base + c, rr);
-    } else {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) rr[i] = 0.f;
+  for (int i = 0; i < NCH; ++i) {
+    const int c = lane * 8 + 256 * i;
+    if (c < d) {
+      float gg[8], rr[8];
+      load8(g + c, gg);
+      if (resid) {
+        load8(resid + base + c, rr);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) rr[e] = 0.f;
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) rr[e] += r * gg[e] * a[i][e] - b[i][e] * k;
+      float4* o = reinterpret_cast<float4*>(out + base + c);
+      o[0] = make_float4(rr[0], rr[1], rr[2], rr[3]);
+      o[1] = make_float4(rr[4], rr[5], rr[6], rr[7]);
+      if (oh) store8(oh, ol, base + c, rr);
     }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) rr[i] += r * gg[i] * a[i] - b[i] * k;
-    float4* o = reinterpret_cast<float4*>(out + base + c);
-    o[0] = make_float4(rr[0], rr[1], rr[2], rr[3]);
-    o[1] = make_float4(rr[4], rr[5], rr[6], rr[7]);
-    if (oh) store8(oh, ol, base + c, rr);
   }
 }
 
@@ -363,16 +383,48 @@ int rows_targets(const int* tok, int n, const int* next, int V, int* tgt, int* e
   return (int)cudaGetLastError();
 }
 
+// Row kernels of the norm: 4 warps (4 rows) per block, per-lane register chunks
+// of 8 columns; d % 8 == 0 and d <= 256 * kNormMaxChunks.
+constexpr int kNormWarps = 4;
+constexpr int kNormMaxChunks = 16;
+
+template <int NCH>
+int norm_fwd_n(const float* x, const float* g, float eps, int n, int d, bf16* yh, bf16* yl, float* rstd,
+               cudaStream_t st) {
+  if constexpr (NCH > kNormMaxChunks) {
+    return (int)cudaErrorInvalidValue;
+  } else {
+    if ((d + 255) / 256 > NCH) return norm_fwd_n<NCH + 1>(x, g, eps, n, d, yh, yl, rstd, st);
+    rmsnorm_kernel<NCH><<<(n + kNormWarps - 1) / kNormWarps, kNormWarps * 32, 0, st>>>(x, g, eps, n, d, yh, yl, rstd);
+    return (int)cudaGetLastError();
+  }
+}
+
+template <int NCH>
+int norm_bwd_n(const float* dy, const float* x, const float* g, const float* rstd, const float* resid, int n, int d,
+               float* out, bf16* oh, bf16* ol, cudaStream_t st) {
+  if constexpr (NCH > kNormMaxChunks) {
+    return (int)cudaErrorInvalidValue;
+  } else {
+    if ((d + 255) / 256 > NCH) return norm_bwd_n<NCH + 1>(dy, x, g, rstd, resid, n, d, out, oh, ol, st);
+    rmsnorm_bwd_kernel<NCH><<<(n + kNormWarps - 1) / kNormWarps, kNormWarps * 32, 0, st>>>(dy, x, g, rstd, resid, n,
+                                                                                           d, out, oh, ol);
+    return (int)cudaGetLastError();
+  }
+}
+
 int rows_rmsnorm(const float* x, const float* g, float eps, int n, int d, bf16* yh, bf16* yl, float* rstd,
                  cudaStream_t st) {
-  rmsnorm_kernel<<<row_grid(n), kRowWarps * 32, 0, st>>>(x, g, eps, n, d, yh, yl, rstd);
-  return (int)cudaGetLastError();
+  if (n <= 0) return 0;
+  if (d % 8) return (int)cudaErrorInvalidValue;
+  return norm_fwd_n<1>(x, g, eps, n, d, yh, yl, rstd, st);
 }
 
 int rows_rmsnorm_bwd(const float* dy, const float* x, const float* g, const float* rstd, const float* resid, int n,
                      int d, float* out, bf16* oh, bf16* ol, cudaStream_t st) {
-  rmsnorm_bwd_kernel<<<row_grid(n), kRowWarps * 32, 0, st>>>(dy, x, g, rstd, resid, n, d, out, oh, ol);
-  return (int)cudaGetLastError();
+  if (n <= 0) return 0;
+  if (d % 8) return (int)cudaErrorInvalidValue;
+  return norm_bwd_n<1>(dy, x, g, rstd, resid, n, d, out, oh, ol, st);
 }
 
 int rows_rope_table(long pos0, int n, int dh, const double* inv_freq, float* cs, float* sn, cudaStream_t st) {

@@ -61,6 +61,7 @@ struct ttt_ctx {
   bool split = false, loaded = false;
   std::string err;
   int L = 0, S = 0, d = 0, H = 0, dh = 0, f = 0, V = 0, k = 0, b = 0, B = 0;
+  int G = 1, R = 0;  // chunks per frozen-prefix pass, and its rows G*b
   std::vector<void*> allocs;
   // frozen weights
   float* E = nullptr;        // [V][d]
@@ -72,9 +73,9 @@ struct ttt_ctx {
   float* loss_dev = nullptr;
   double* inv_freq = nullptr;
   float *cs = nullptr, *sn = nullptr;
-  float *x = nullptr, *qkv = nullptr, *a = nullptr;
+  float *x = nullptr, *xp = nullptr, *qkv = nullptr;
   Pair xn, q, o, u;
-  Pair kown, vown;           // [L][b][d]
+  Pair kown, vown;           // [L][R][d]
   float *sx = nullptr, *sh = nullptr, *srs_a = nullptr, *srs_m = nullptr, *slse = nullptr, *sa = nullptr;
   Pair sq, so, sxm, su;
   Pair xf, dz;
@@ -86,7 +87,7 @@ struct ttt_ctx {
   float *init_up = nullptr, *init_down = nullptr;
   // launch counting and optional per-class event timing
   int64_t launches = 0;
-  bool prof_on = false;
+  uint64_t prof_mask = 0;   // bit i: bracket launches of kernel class i with events
   std::vector<cudaEvent_t> ev_pool;
   size_t ev_used = 0;
   struct ProfRec {
@@ -105,6 +106,9 @@ struct ttt_ctx {
 using ProfRec = ttt_ctx::ProfRec;
 
 namespace {
+
+// Rows of one frozen-prefix pass (whole chunks): large enough for full GEMM waves.
+constexpr int kPrefixRows = 4096;
 
 int fail(ttt_ctx* c, int code, const std::string& msg) {
   if (c) c->err = msg;
@@ -190,7 +194,7 @@ cudaEvent_t next_event(ttt_ctx* c) {
 template <class F>
 int site(ttt_ctx* c, int cls, int nkern, double alg, double exec, double bytes, F&& f) {
   cudaEvent_t a = nullptr;
-  if (c->prof_on && (a = next_event(c))) cudaEventRecord(a, c->st);
+  if (((c->prof_mask >> cls) & 1u) && (a = next_event(c))) cudaEventRecord(a, c->st);
   const int r = f();
   if (a) {
     cudaEvent_t b = next_event(c);
@@ -216,11 +220,138 @@ long attn_tiles(long pos0, int n, int k, int qt) {
   return ring + (qend - 1) / 128 + 1;
 }
 
-// One inner-loop step of sequence s: tokens tok[n] / next target next[1] on the device.
-int step(ttt_ctx* c, int s, const int* tok, int n, const int* next, float* loss_out) {
+// Window pairs (query, visible key) of n queries starting at absolute position pos0.
+double window_pairs(long pos0, int n, int k) {
+  double pairs = 0;
+  for (long p = pos0; p < pos0 + n; ++p) pairs += (double)std::min<long>(p + 1, k);
+  return pairs;
+}
+double tile_pairs(long pos0, int n, int k) {
+  double t = 0;
+  for (int qt = 0; qt < (n + 127) / 128; ++qt) t += 128.0 * 128.0 * attn_tiles(pos0, n, k, qt);
+  return t;
+}
+
+// Forward of block l over n rows at absolute positions pos0..pos0+n-1.  Frozen
+// blocks update the residual stream xin in place; trainable blocks (si >= 0)
+// keep what their backward needs in the suffix buffers and write xout.
+int layer_forward(ttt_ctx* c, Seq& sq_, int l, int si, int n, long pos0, float* xin, float* xout,
+                  const float* cs, const float* sn) {
+  cudaStream_t st = c->st;
+  const int d = c->d, H = c->H, dh = c->dh, f = c->f, k = c->k, b = c->b, R = c->R;
+  const bool suf = si >= 0, sp = c->split;
+  const double nn = n, dd = d, ff = f;
+  const double ops = sp ? 3.0 : 1.0, eb = sp ? 4.0 : 2.0;
+  float* hbuf = suf ? c->sh + (long)si * b * d : xin;
+  Pair xn_a = c->xn;
+  Pair qb = suf ? c->sq.at((long)si * b * d) : c->q;
+  Pair ob = suf ? c->so.at((long)si * b * d) : c->o;
+  Pair xn_m = suf ? c->sxm.at((long)si * b * d) : c->xn;
+  Pair ub = suf ? c->su.at((long)si * b * f) : c->u;
+  Pair ko = c->kown.at((long)l * R * d), vo = c->vown.at((long)l * R * d);
+  Pair kr = sq_.ring_k.at((long)l * k * d), vr = sq_.ring_v.at((long)l * k * d);
+
+  RUN(K_RMSNORM, 1, 0, 0, nn * dd * (4 + eb),
+      rows_rmsnorm(xin, c->gains + (long)(2 * l) * d, c->cfg.rms_eps, n, d, xn_a.hi, xn_a.lo,
+                   suf ? c->srs_a + (long)si * b : nullptr, st));
+  if (qkv_rope_bn(dh, d, sp)) {  // RoPE and the q / own k / own v writes fused into the product's epilogue
+    GemmArgs g;
+    g.M = n; g.N = 3 * d; g.K = d; g.err = c->derr;
+    g.rq_h = qb.hi; g.rq_l = qb.lo; g.rk_h = ko.hi; g.rk_l = ko.lo; g.rv_h = vo.hi; g.rv_l = vo.lo;
+    g.rcs = cs; g.rsn = sn; g.rd = d;
+    RUN(K_GEMM_QKV, 1, 6 * nn * dd * dd, 6 * nn * dd * dd * ops, 0,
+        gemm_qkv_rope(opnd(xn_a, d, 0), opnd(c->Wqkv.at((long)l * d * 3 * d), 3 * d, 1), g, dh, sp, st));
+  } else {
+    GemmArgs g;
+    g.M = n; g.N = 3 * d; g.K = d;
+    g.out32 = c->qkv; g.ldo32 = 3 * d; g.err = c->derr;
+    RUN(K_GEMM_QKV, 1, 6 * nn * dd * dd, 6 * nn * dd * dd * ops, 0,
+        gemm_run(EPI_F32, opnd(xn_a, d, 0), opnd(c->Wqkv.at((long)l * d * 3 * d), 3 * d, 1), g, sp, st));
+    RUN(K_ROPE, 1, 0, 0, nn * dd * (12 + 3 * eb),
+        rows_rope_qkv(c->qkv, cs, sn, n, H, dh, qb.hi, qb.lo, ko.hi, ko.lo, vo.hi, vo.lo, st));
+  }
+  {
+    AttnMaps m;
+    if (!attn_maps(&m, qb, kr, vr, ko, vo, n, d, k)) return fail(c, TTT_ERR_CUDA, "attention tensor maps");
+    AttnArgs a;
+    a.n = n; a.H = H; a.dh = dh; a.window = k; a.pos0 = pos0;
+    a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)dh));
+    a.o_hi = ob.hi; a.o_lo = ob.lo; a.ldo = d;
+    a.lse = suf ? c->slse + (long)si * H * b : nullptr;
+    a.err = c->derr;
+    RUN(K_ATTN_FWD, 1, 4 * dd * window_pairs(pos0, n, k), 4 * dd * tile_pairs(pos0, n, k) * ops, 0,
+        attn_fwd_run(m, a, sp, st));
+  }
+  {
+    GemmArgs g;
+    g.M = n; g.N = d; g.K = d;
+    g.out32 = hbuf; g.ldo32 = d; g.resid = xin; g.ldr = d; g.err = c->derr; g.allow_ksplit = true;
+    RUN(K_GEMM_O, 1, 2 * nn * dd * dd, 2 * nn * dd * dd * ops, 0,
+        gemm_run(EPI_RESID, opnd(ob, d, 0), opnd(c->Wo.at((long)l * d * d), d, 1), g, sp, st));
+  }
+  RUN(K_RMSNORM, 1, 0, 0, nn * dd * (4 + eb),
+      rows_rmsnorm(hbuf, c->gains + (long)(2 * l + 1) * d, c->cfg.rms_eps, n, d, xn_m.hi, xn_m.lo,
+                   suf ? c->srs_m + (long)si * b : nullptr, st));
+  {
+    GemmArgs g;
+    g.M = n; g.N = f; g.K = d;
+    g.out32 = suf ? c->sa + (long)si * b * f : nullptr;  // pre-activation kept for GELU' only when trainable
+    g.ldo32 = f; g.oh = ub.hi; g.ol = ub.lo; g.ldo = f; g.err = c->derr;
+    Pair w = suf ? sq_.up16.at((long)si * d * f) : c->Wup.at((long)l * d * f);
+    RUN(K_GEMM_UP, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 0,
+        gemm_run(EPI_GELU, opnd(xn_m, d, 0), opnd(w, f, 1), g, sp, st));
+  }
+  {
+    GemmArgs g;
+    g.M = n; g.N = d; g.K = f;
+    g.out32 = xout; g.ldo32 = d; g.resid = hbuf; g.ldr = d; g.err = c->derr; g.allow_ksplit = true;
+    Pair w = suf ? sq_.down16.at((long)si * f * d) : c->Wdown.at((long)l * f * d);
+    RUN(K_GEMM_DOWN, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 0,
+        gemm_run(EPI_RESID, opnd(ub, f, 0), opnd(w, d, 1), g, sp, st));
+  }
+  return TTT_OK;
+}
+
+// The frozen blocks 0..L-S-1 of sequence s over n tokens (whole chunks, n <= R)
+// starting at absolute position pos0.  Their outputs do not depend on the fast
+// weights, so several chunks go through them in one pass; the suffix steps of
+// those chunks then read their rows of c->xp.  The frozen blocks' keys/values
+// of all n tokens enter the window cache at the end of the pass (every query of
+// the pass has already read the cache).
+int prefix_pass(ttt_ctx* c, int s, const int* tok, int n, long pos0) {
   Seq& sq_ = c->seqs[s];
   cudaStream_t st = c->st;
-  const int L = c->L, S = c->S, d = c->d, H = c->H, dh = c->dh, f = c->f, V = c->V, k = c->k, b = c->b;
+  const int d = c->d, dh = c->dh, k = c->k, R = c->R;
+  const int P0 = c->L - c->S;
+  const double nn = n, dd = d;
+  RUN(K_MISC, 1, 0, 0, nn * dd * 8, rows_embed(tok, n, c->E, c->V, d, c->xp, c->derr, st));
+  RUN(K_ROPE, 1, 0, 0, nn * dh * 4, rows_rope_table(pos0, n, dh, c->inv_freq, c->cs, c->sn, st));
+  for (int l = 0; l < P0; ++l) {
+    const int r = layer_forward(c, sq_, l, -1, n, pos0, c->xp, c->xp, c->cs, c->sn);
+    if (r != TTT_OK) return r;
+  }
+  if (P0 > 0) {
+    const double cb = (double)P0 * nn * dd * 2 * 2;
+    RUN(K_COMMIT, 1, 0, 0, cb, rows_commit(c->kown.hi, sq_.ring_k.hi, (long)R * d, (long)k * d, P0, pos0, n, k, d, st));
+    RUN(K_COMMIT, 1, 0, 0, cb, rows_commit(c->vown.hi, sq_.ring_v.hi, (long)R * d, (long)k * d, P0, pos0, n, k, d, st));
+    if (c->split) {
+      RUN(K_COMMIT, 1, 0, 0, cb,
+          rows_commit(c->kown.lo, sq_.ring_k.lo, (long)R * d, (long)k * d, P0, pos0, n, k, d, st));
+      RUN(K_COMMIT, 1, 0, 0, cb,
+          rows_commit(c->vown.lo, sq_.ring_v.lo, (long)R * d, (long)k * d, P0, pos0, n, k, d, st));
+    }
+  }
+  return TTT_OK;
+}
+
+// One inner-loop step of sequence s for the chunk whose rows start at `row`
+// within the last prefix pass: tokens tok[n], next target next[1] (device).
+// Runs the trainable blocks forward, the loss, the backward through them with
+// the fused SGD step, and commits their keys/values; the position advances by n.
+int suffix_step(ttt_ctx* c, int s, int row, const int* tok, int n, const int* next, float* loss_out) {
+  Seq& sq_ = c->seqs[s];
+  cudaStream_t st = c->st;
+  const int L = c->L, S = c->S, d = c->d, H = c->H, dh = c->dh, f = c->f, V = c->V, k = c->k, b = c->b, R = c->R;
   const long pos0 = sq_.pos;
   const bool sp = c->split;
   const int P0 = L - S;  // first trainable block
@@ -228,95 +359,22 @@ int step(ttt_ctx* c, int s, const int* tok, int n, const int* next, float* loss_
   const double nn = n, dd = d, ff = f, VV = V;
   const double ops = sp ? 3.0 : 1.0;             // products per multiply in split mode
   const double eb = sp ? 4.0 : 2.0;              // bytes per operand element (hi [+ lo])
-
-  // algorithmic work of this chunk's attention: window pairs and own-chunk causal pairs
-  double pairs = 0, tile_pairs = 0;
-  for (long p = pos0; p < pos0 + n; ++p) pairs += (double)std::min<long>(p + 1, k);
+  const double pairs = window_pairs(pos0, n, k), tpairs = tile_pairs(pos0, n, k);
   const double own_pairs = nn * (nn + 1) / 2;
-  for (int qt = 0; qt < (n + 127) / 128; ++qt) tile_pairs += 128.0 * 128.0 * attn_tiles(pos0, n, k, qt);
   const int nq = (n + 127) / 128;
   const double own_tile_pairs = 128.0 * 128.0 * nq * (nq + 1) / 2;
+  const float* cs = c->cs + (long)row * (dh / 2);
+  const float* sn = c->sn + (long)row * (dh / 2);
 
   RUN(K_MISC, 1, 0, 0, nn * 8, rows_targets(tok, n, next, V, c->tgt, c->derr, st));
-  RUN(K_MISC, 1, 0, 0, nn * dd * 8, rows_embed(tok, n, c->E, V, d, c->x, c->derr, st));
-  RUN(K_ROPE, 1, 0, 0, nn * dh * 4, rows_rope_table(pos0, n, dh, c->inv_freq, c->cs, c->sn, st));
-
-  auto in_ptr = [&](int l) -> float* { return l >= P0 ? c->sx + (long)(l - P0) * b * d : c->x; };
-
-  AttnArgs aa;
-  aa.n = n;
-  aa.H = H;
-  aa.dh = dh;
-  aa.window = k;
-  aa.pos0 = pos0;
-  aa.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)dh));
-  aa.ldo = d;
-  aa.err = c->derr;
 
   // ------------------------------------------------------------------ forward
-  if (P0 == 0) CK(cudaMemcpyAsync(c->sx, c->x, (size_t)n * d * 4, cudaMemcpyDeviceToDevice, st));
-  for (int l = 0; l < L; ++l) {
-    const bool suf = l >= P0;
+  for (int l = P0; l < L; ++l) {
     const int si = l - P0;
-    float* xin = in_ptr(l);
-    float* xout = (l + 1 < L) ? in_ptr(l + 1) : c->x;
-    float* hbuf = suf ? c->sh + (long)si * b * d : xin;
-    Pair xn_a = c->xn;
-    Pair qb = suf ? c->sq.at((long)si * b * d) : c->q;
-    Pair ob = suf ? c->so.at((long)si * b * d) : c->o;
-    Pair xn_m = suf ? c->sxm.at((long)si * b * d) : c->xn;
-    float* abuf = suf ? c->sa + (long)si * b * f : c->a;
-    Pair ub = suf ? c->su.at((long)si * b * f) : c->u;
-    Pair ko = c->kown.at((long)l * b * d), vo = c->vown.at((long)l * b * d);
-    Pair kr = sq_.ring_k.at((long)l * k * d), vr = sq_.ring_v.at((long)l * k * d);
-
-    RUN(K_RMSNORM, 1, 0, 0, nn * dd * (4 + eb),
-        rows_rmsnorm(xin, c->gains + (long)(2 * l) * d, c->cfg.rms_eps, n, d, xn_a.hi, xn_a.lo,
-                     suf ? c->srs_a + (long)si * b : nullptr, st));
-    {
-      GemmArgs g;
-      g.M = n; g.N = 3 * d; g.K = d;
-      g.out32 = c->qkv; g.ldo32 = 3 * d; g.err = c->derr;
-      RUN(K_GEMM_QKV, 1, 6 * nn * dd * dd, 6 * nn * dd * dd * ops, 0,
-          gemm_run(EPI_F32, opnd(xn_a, d, 0), opnd(c->Wqkv.at((long)l * d * 3 * d), 3 * d, 1), g, sp, st));
-    }
-    RUN(K_ROPE, 1, 0, 0, nn * dd * (12 + 3 * eb),
-        rows_rope_qkv(c->qkv, c->cs, c->sn, n, H, dh, qb.hi, qb.lo, ko.hi, ko.lo, vo.hi, vo.lo, st));
-    {
-      AttnMaps m;
-      if (!attn_maps(&m, qb, kr, vr, ko, vo, n, d, k)) return fail(c, TTT_ERR_CUDA, "attention tensor maps");
-      AttnArgs a2 = aa;
-      a2.o_hi = ob.hi;
-      a2.o_lo = ob.lo;
-      a2.lse = suf ? c->slse + (long)si * H * b : nullptr;
-      RUN(K_ATTN_FWD, 1, 4 * dd * pairs, 4 * dd * tile_pairs * ops, 0, attn_fwd_run(m, a2, sp, st));
-    }
-    {
-      GemmArgs g;
-      g.M = n; g.N = d; g.K = d;
-      g.out32 = hbuf; g.ldo32 = d; g.resid = xin; g.ldr = d; g.err = c->derr;
-      RUN(K_GEMM_O, 1, 2 * nn * dd * dd, 2 * nn * dd * dd * ops, 0,
-          gemm_run(EPI_RESID, opnd(ob, d, 0), opnd(c->Wo.at((long)l * d * d), d, 1), g, sp, st));
-    }
-    RUN(K_RMSNORM, 1, 0, 0, nn * dd * (4 + eb),
-        rows_rmsnorm(hbuf, c->gains + (long)(2 * l + 1) * d, c->cfg.rms_eps, n, d, xn_m.hi, xn_m.lo,
-                     suf ? c->srs_m + (long)si * b : nullptr, st));
-    {
-      GemmArgs g;
-      g.M = n; g.N = f; g.K = d;
-      g.out32 = abuf; g.ldo32 = f; g.oh = ub.hi; g.ol = ub.lo; g.ldo = f; g.err = c->derr;
-      Pair w = suf ? sq_.up16.at((long)si * d * f) : c->Wup.at((long)l * d * f);
-      RUN(K_GEMM_UP, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 0,
-          gemm_run(EPI_GELU, opnd(xn_m, d, 0), opnd(w, f, 1), g, sp, st));
-    }
-    {
-      GemmArgs g;
-      g.M = n; g.N = d; g.K = f;
-      g.out32 = xout; g.ldo32 = d; g.resid = hbuf; g.ldr = d; g.err = c->derr;
-      Pair w = suf ? sq_.down16.at((long)si * f * d) : c->Wdown.at((long)l * f * d);
-      RUN(K_GEMM_DOWN, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 0,
-          gemm_run(EPI_RESID, opnd(ub, f, 0), opnd(w, d, 1), g, sp, st));
-    }
+    float* xin = si == 0 ? c->xp + (long)row * d : c->sx + (long)si * b * d;
+    float* xout = (l + 1 < L) ? c->sx + (long)(si + 1) * b * d : c->x;
+    const int r = layer_forward(c, sq_, l, si, n, pos0, xin, xout, cs, sn);
+    if (r != TTT_OK) return r;
   }
   // final norm + LM head + cross-entropy statistics
   RUN(K_RMSNORM, 1, 0, 0, nn * dd * (4 + eb),
@@ -346,7 +404,7 @@ int step(ttt_ctx* c, int s, const int* tok, int n, const int* next, float* loss_
   {
     GemmArgs g;
     g.M = n; g.N = d; g.K = V;
-    g.out32 = c->dxn; g.ldo32 = d; g.err = c->derr;
+    g.out32 = c->dxn; g.ldo32 = d; g.err = c->derr; g.allow_ksplit = true;
     RUN(K_LM_DX, 1, 2 * nn * dd * VV, 2 * nn * dd * VV * ops, 0,
         gemm_run(EPI_F32, opnd(c->dz, V, 0), opnd(c->Wlm, V, 0), g, sp, st));
   }
@@ -375,7 +433,7 @@ int step(ttt_ctx* c, int s, const int* tok, int n, const int* next, float* loss_
     if (si > 0) {  // dXn_m = dA W_up^T  (before W_up changes)
       GemmArgs g;
       g.M = n; g.N = d; g.K = f;
-      g.out32 = c->dxn; g.ldo32 = d; g.err = c->derr;
+      g.out32 = c->dxn; g.ldo32 = d; g.err = c->derr; g.allow_ksplit = true;
       RUN(K_MLP_DX, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 0,
           gemm_run(EPI_F32, opnd(c->da, f, 0), opnd(up16, f, 0), g, sp, st));
     }
@@ -404,7 +462,7 @@ int step(ttt_ctx* c, int s, const int* tok, int n, const int* next, float* loss_
         rows_attn_rowdot(c->do16.hi, c->do16.lo, ob.hi, ob.lo, n, H, dh, c->D, st));
     {
       AttnBwdMaps m;
-      Pair ko = c->kown.at((long)l * b * d), vo = c->vown.at((long)l * b * d);
+      Pair ko = c->kown.at((long)l * R * d), vo = c->vown.at((long)l * R * d);
       Pair kr = sq_.ring_k.at((long)l * k * d), vr = sq_.ring_v.at((long)l * k * d);
       if (!attn_maps(&m.f, qb, kr, vr, ko, vo, n, d, k) ||
           !make_map(&m.dO, c->do16.hi, (uint64_t)d, (uint64_t)n, d, 128))
@@ -416,7 +474,9 @@ int step(ttt_ctx* c, int s, const int* tok, int n, const int* next, float* loss_
         m.dOl = m.dO;
       }
       AttnBwdArgs ba;
-      ba.g = aa;
+      ba.g.n = n; ba.g.H = H; ba.g.dh = dh; ba.g.window = k; ba.g.pos0 = pos0;
+      ba.g.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)dh));
+      ba.g.ldo = d; ba.g.err = c->derr;
       ba.lse = c->slse + (long)si * H * b;
       ba.D = c->D;
       ba.dq = c->dq;
@@ -424,15 +484,15 @@ int step(ttt_ctx* c, int s, const int* tok, int n, const int* next, float* loss_
       ba.dv = c->dv;
       ba.ldg = d;
       ba.scale = (float)(1.0 / std::sqrt((double)dh));
-      RUN(K_ATTN_DQ, 1, 4 * dd * pairs, 6 * dd * tile_pairs * ops, 0, attn_bwd_run(m, ba, sp, st, 1));
+      RUN(K_ATTN_DQ, 1, 4 * dd * pairs, 6 * dd * tpairs * ops, 0, attn_bwd_run(m, ba, sp, st, 1));
       RUN(K_ATTN_DKV, 1, 4 * dd * own_pairs, 8 * dd * own_tile_pairs * ops, 0, attn_bwd_run(m, ba, sp, st, 2));
     }
     RUN(K_ROPE, 1, 0, 0, nn * dd * (12 + 3 * eb),
-        rows_rope_bwd(c->dq, c->dk, c->dv, c->cs, c->sn, n, H, dh, c->dqkv.hi, c->dqkv.lo, st));
+        rows_rope_bwd(c->dq, c->dk, c->dv, cs, sn, n, H, dh, c->dqkv.hi, c->dqkv.lo, st));
     {  // dXn_a = dQKV Wqkv^T
       GemmArgs g;
       g.M = n; g.N = d; g.K = 3 * d;
-      g.out32 = c->dxn; g.ldo32 = d; g.err = c->derr;
+      g.out32 = c->dxn; g.ldo32 = d; g.err = c->derr; g.allow_ksplit = true;
       RUN(K_ATTN_DX, 1, 6 * nn * dd * dd, 6 * nn * dd * dd * ops, 0,
           gemm_run(EPI_F32, opnd(c->dqkv, 3 * d, 0), opnd(c->Wqkv.at((long)l * d * 3 * d), 3 * d, 0), g, sp, st));
     }
@@ -442,14 +502,17 @@ int step(ttt_ctx* c, int s, const int* tok, int n, const int* next, float* loss_
                          c->dh32, n, d, c->dy, c->dy16.hi, c->dy16.lo, st));
   }
   // ------------------------------------------------------------------- commit
-  const double cb = (double)L * nn * dd * 2 * 2;
-  RUN(K_COMMIT, 1, 0, 0, cb, rows_commit(c->kown.hi, sq_.ring_k.hi, (long)b * d, (long)k * d, L, pos0, n, k, d, st));
-  RUN(K_COMMIT, 1, 0, 0, cb, rows_commit(c->vown.hi, sq_.ring_v.hi, (long)b * d, (long)k * d, L, pos0, n, k, d, st));
+  const double cb = (double)S * nn * dd * 2 * 2;
+  const long os = (long)R * d, rs = (long)k * d;
+  RUN(K_COMMIT, 1, 0, 0, cb,
+      rows_commit(c->kown.hi + (long)P0 * os, sq_.ring_k.hi + (long)P0 * rs, os, rs, S, pos0, n, k, d, st));
+  RUN(K_COMMIT, 1, 0, 0, cb,
+      rows_commit(c->vown.hi + (long)P0 * os, sq_.ring_v.hi + (long)P0 * rs, os, rs, S, pos0, n, k, d, st));
   if (sp) {
     RUN(K_COMMIT, 1, 0, 0, cb,
-        rows_commit(c->kown.lo, sq_.ring_k.lo, (long)b * d, (long)k * d, L, pos0, n, k, d, st));
+        rows_commit(c->kown.lo + (long)P0 * os, sq_.ring_k.lo + (long)P0 * rs, os, rs, S, pos0, n, k, d, st));
     RUN(K_COMMIT, 1, 0, 0, cb,
-        rows_commit(c->vown.lo, sq_.ring_v.lo, (long)b * d, (long)k * d, L, pos0, n, k, d, st));
+        rows_commit(c->vown.lo + (long)P0 * os, sq_.ring_v.lo + (long)P0 * rs, os, rs, S, pos0, n, k, d, st));
   }
   sq_.pos = pos0 + n;
   return TTT_OK;
@@ -467,7 +530,8 @@ extern "C" int ttt_create(const ttt_config* cfg, void* cuda_stream, ttt_ctx** ou
     return TTT_ERR_ARG;
   const int dh = g.d_model / g.n_heads;
   const bool split = g.compute == 0;
-  if (dh % 16 || dh > 128 || (split && dh > 64) || g.d_model % 64 || g.d_ff % 64 || g.vocab % 8 || g.window % 128)
+  if (dh % 16 || dh > 128 || (split && dh > 64) || g.d_model % 64 || g.d_model > 4096 || g.d_ff % 64 ||
+      g.vocab % 8 || g.window % 128)
     return TTT_ERR_UNSUPPORTED;
   ttt_ctx* c = new ttt_ctx();
   c->cfg = g;
@@ -475,6 +539,9 @@ extern "C" int ttt_create(const ttt_config* cfg, void* cuda_stream, ttt_ctx** ou
   c->split = split;
   c->L = g.n_layers; c->S = g.n_trainable; c->d = g.d_model; c->H = g.n_heads; c->dh = dh; c->f = g.d_ff;
   c->V = g.vocab; c->k = g.window; c->b = g.chunk; c->B = g.n_seqs;
+  // the frozen blocks run ahead over up to kPrefixRows tokens of whole chunks, never more than the window
+  c->G = std::max(1, std::min(kPrefixRows / c->b, c->k / c->b));
+  c->R = c->G * c->b;
   const long L = c->L, S = c->S, d = c->d, f = c->f, V = c->V, k = c->k, b = c->b, H = c->H;
   bool ok = true;
   c->E = dalloc<float>(c, V * d, ok);
@@ -503,17 +570,18 @@ extern "C" int ttt_create(const ttt_config* cfg, void* cuda_stream, ttt_ctx** ou
   c->derr = dalloc<int>(c, 1, ok);
   c->loss_dev = dalloc<float>(c, g.n_seqs, ok);
   c->inv_freq = dalloc<double>(c, dh / 2, ok);
-  c->cs = dalloc<float>(c, b * dh / 2, ok);
-  c->sn = dalloc<float>(c, b * dh / 2, ok);
+  const long R = c->R;
+  c->cs = dalloc<float>(c, R * dh / 2, ok);
+  c->sn = dalloc<float>(c, R * dh / 2, ok);
   c->x = dalloc<float>(c, b * d, ok);
-  c->qkv = dalloc<float>(c, b * 3 * d, ok);
-  c->a = dalloc<float>(c, b * f, ok);
-  c->xn = palloc(c, b * d, ok);
-  c->q = palloc(c, b * d, ok);
-  c->o = palloc(c, b * d, ok);
-  c->u = palloc(c, b * f, ok);
-  c->kown = palloc(c, L * b * d, ok);
-  c->vown = palloc(c, L * b * d, ok);
+  c->xp = dalloc<float>(c, R * d, ok);
+  c->qkv = dalloc<float>(c, R * 3 * d, ok);
+  c->xn = palloc(c, R * d, ok);
+  c->q = palloc(c, R * d, ok);
+  c->o = palloc(c, R * d, ok);
+  c->u = palloc(c, R * f, ok);
+  c->kown = palloc(c, L * R * d, ok);
+  c->vown = palloc(c, L * R * d, ok);
   c->sx = dalloc<float>(c, S * b * d, ok);
   c->sh = dalloc<float>(c, S * b * d, ok);
   c->srs_a = dalloc<float>(c, S * b, ok);
@@ -679,7 +747,9 @@ extern "C" int ttt_prefill_chunk_dev(ttt_ctx* c, const int32_t* d_tokens, int32_
   if (!c->loaded) return fail(c, TTT_ERR_STATE, "weights not loaded");
   if (n < 1 || n > c->b) return fail(c, TTT_ERR_ARG, "n outside 1..chunk");
   for (int s = 0; s < c->B; ++s) {
-    const int r = step(c, s, d_tokens + (long)s * n, n, d_next + s, d_loss + s);
+    const int32_t* tk = d_tokens + (long)s * n;
+    int r = prefix_pass(c, s, tk, n, c->seqs[s].pos);
+    if (r == TTT_OK) r = suffix_step(c, s, 0, tk, n, d_next + s, d_loss + s);
     if (r != TTT_OK) return r;
   }
   return TTT_OK;
@@ -710,13 +780,19 @@ extern "C" int ttt_prefill_sequence_dev(ttt_ctx* c, const int32_t* d_tokens, int
   if (!c->loaded) return fail(c, TTT_ERR_STATE, "weights not loaded");
   const int b = c->b;
   const int nc = (T + b - 1) / b;
-  for (int ci = 0; ci < nc; ++ci) {
-    const int s0 = ci * b, n = std::min(b, T - s0);
+  for (int g0 = 0; g0 < nc; g0 += c->G) {  // one frozen-prefix pass per group of G chunks
+    const int g1 = std::min(nc, g0 + c->G);
+    const int t0 = g0 * b, t1 = std::min(T, g1 * b);
     for (int s = 0; s < c->B; ++s) {
-      const int32_t* tk = d_tokens + (long)s * T + s0;
-      const int32_t* nx = (s0 + n < T) ? tk + n : c->minus1;
-      const int r = step(c, s, tk, n, nx, d_losses + (long)s * nc + ci);
+      const int32_t* seq = d_tokens + (long)s * T;
+      int r = prefix_pass(c, s, seq + t0, t1 - t0, c->seqs[s].pos);
       if (r != TTT_OK) return r;
+      for (int ci = g0; ci < g1; ++ci) {
+        const int s0 = ci * b, n = std::min(b, T - s0);
+        const int32_t* nx = (s0 + n < T) ? seq + s0 + n : c->minus1;
+        r = suffix_step(c, s, s0 - t0, seq + s0, n, nx, d_losses + (long)s * nc + ci);
+        if (r != TTT_OK) return r;
+      }
     }
   }
   return TTT_OK;
@@ -759,14 +835,18 @@ extern "C" int ttt_reset(ttt_ctx* c) {
 
 extern "C" int64_t ttt_launch_count(const ttt_ctx* c) { return c ? c->launches : -1; }
 
-extern "C" int ttt_profile(ttt_ctx* c, int enable) {
+extern "C" int ttt_profile(ttt_ctx* c, int64_t class_mask) {
   if (!c) return TTT_ERR_ARG;
   if (cudaStreamSynchronize(c->st) != cudaSuccess) return fail(c, TTT_ERR_CUDA, "stream synchronize");
   c->recs.clear();
   c->ev_used = 0;
   for (auto& a : c->acc) a = ttt_ctx::ProfAcc();
-  c->prof_on = enable != 0;
+  c->prof_mask = (uint64_t)class_mask & ((1ull << K_NCLS) - 1);
   return TTT_OK;
+}
+
+extern "C" const char* ttt_profile_class_name(int cls) {
+  return (cls >= 0 && cls < K_NCLS) ? kClsName[cls] : nullptr;
 }
 
 extern "C" int ttt_profile_read(ttt_ctx* c, ttt_kernel_stat* out, int max_out, int* n_out) {

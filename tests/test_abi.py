@@ -59,7 +59,7 @@ int main(void) {
   F(ttt_kernel_stat, launches) F(ttt_kernel_stat, ms) F(ttt_kernel_stat, bytes)
   printf("ttt_gemm_epilogue %zu\n", sizeof(ttt_gemm_epilogue));
   F(ttt_gemm_epilogue, ldo) F(ttt_gemm_epilogue, eta) F(ttt_gemm_epilogue, tgt) F(ttt_gemm_epilogue, scale)
-  F(ttt_gemm_epilogue, err)
+  F(ttt_gemm_epilogue, err) F(ttt_gemm_epilogue, allow_ksplit)
   return 0;
 }
 """

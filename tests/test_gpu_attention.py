@@ -47,6 +47,8 @@ CASES = [  # n, H, dh, window, pos0, split
     (64, 4, 32, 128, 448, True),
     (100, 2, 64, 128, 300, True),
     (37, 2, 64, 256, 700, False),
+    (512, 2, 96, 1024, 1500, False),   # two 256-query blocks, cache wraps, unaligned start
+    (384, 2, 64, 512, 640, False),     # second block half full
 ]
 
 

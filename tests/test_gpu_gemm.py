@@ -177,3 +177,26 @@ def test_gemm_cross_entropy_epilogues(N):
     ref[~ok] = 0
     ref /= ok.sum()
     assert rel(f64(dh) + f64(dl), ref) < 1e-5
+
+
+@pytest.mark.parametrize("M,N,K,a_mn", [(1024, 1536, 6144, 0), (1024, 768, 32000, 0), (300, 200, 2048, 1)])
+def test_gemm_k_slices_f32_and_residual(M, N, K, a_mn):
+    """Under-filled products cut into K slices whose partial sums are added atomically."""
+    a, b, Aq, Bq = operands(M, N, K, a_mn, 1, scale=0.25)
+    ref = Aq @ Bq.T
+    err = errword()
+    out = torch.full((M, N), float("nan"), dtype=torch.float32, device=dev)   # cleared by the call
+    T.gemm(T.EPI_F32, M, N, K, a, b, a_mn=a_mn, b_mn=1, out32=out, ldo32=N, allow_ksplit=1, err=err)
+    x = torch.tensor(RNG.standard_normal((M, N)), dtype=torch.float32, device=dev)
+    x0 = x.cpu().numpy().astype(np.float64)
+    T.gemm(T.EPI_RESID, M, N, K, a, b, a_mn=a_mn, b_mn=1, out32=x, ldo32=N, resid=x, ldr=N, allow_ksplit=1,
+           err=err)                                                           # in place
+    y = torch.full((M, N), float("nan"), dtype=torch.float32, device=dev)
+    T.gemm(T.EPI_RESID, M, N, K, a, b, a_mn=a_mn, b_mn=1, out32=y, ldo32=N, resid=x, ldr=N, allow_ksplit=1,
+           err=err)                                                           # out != resid
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    tol = 1e-6 + 6e-10 * K              # fp32 accumulation of K exact bf16 products (TMEM, then slices)
+    assert rel(out.cpu().numpy(), ref) < tol
+    assert rel(x.cpu().numpy(), x0 + ref) < tol
+    assert rel(y.cpu().numpy(), x0 + 2 * ref) < tol

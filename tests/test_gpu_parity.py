@@ -27,6 +27,8 @@ SMALL = {
     "dh96": Shape(8, 384, 4, 1536, 2048, 256, 256, 1e6, 1e-2, 900),
     "dh128": Shape(8, 512, 4, 2048, 1024, 512, 256, 1e7, 1e-2, 1100),
     "fp32_dh64": Shape(8, 256, 4, 1024, 512, 128, 128, 1e4, 1e-2, 700, compute="fp32"),
+    # the frozen blocks of 4 chunks run as one pass; 10 chunks, the last one ragged
+    "dh96_ahead4": Shape(8, 384, 4, 1536, 2048, 512, 128, 1e6, 1e-2, 1200),
 }
 
 
@@ -49,12 +51,29 @@ def run_gpu(shape, tokens, blob):
     return losses, fw, pos
 
 
-def check(shape, tokens, name):
+def run_gpu_sequence(shape, tokens, blob):
+    """Whole sequence through ttt_prefill_sequence_dev (frozen blocks run ahead over several chunks)."""
+    m = T.TTT.from_shape(shape)
+    m.load_weights(blob)
+    Tn, b = len(tokens), shape.chunk
+    nc = -(-Tn // b)
+    d_tok = torch.tensor(np.asarray(tokens, np.int32), device="cuda")
+    d_loss = torch.zeros(nc, dtype=torch.float32, device="cuda")
+    m.prefill_sequence_dev(d_tok, Tn, d_loss)
+    m.sync()
+    losses = [float(x) for x in d_loss.cpu().numpy()]
+    fw = [m.fast_weights(0, i) for i in range(shape.n_trainable)]
+    pos = m.position
+    m.close()
+    return losses, fw, pos
+
+
+def check(shape, tokens, name, runner=None):
     blob = weight_blob(shape)
     cfg = O.Config.from_shape(shape)
     P = O.unpack(blob, cfg)
     ref_losses, Pf = O.run_sequence(cfg, P, tokens, shape.eta)
-    losses, fw, pos = run_gpu(shape, tokens, blob)
+    losses, fw, pos = (runner or run_gpu)(shape, tokens, blob)
     assert pos == len(tokens)
     tl, tw = TOL[shape.compute]
     lr = [abs(a - b) / abs(b) for a, b in zip(losses, ref_losses)]
@@ -79,6 +98,17 @@ def test_tiny_fp32_full_sequence():
 def test_small_shapes(name):
     s = SMALL[name]
     check(s, zipf_tokens(s.seq_len, s.vocab, seed=1000), name)
+
+
+@pytest.mark.parametrize("name", ["dh64", "dh128", "dh96_ahead4"])
+def test_sequence_api_runs_frozen_blocks_ahead(name):
+    s = SMALL[name]
+    check(s, zipf_tokens(s.seq_len, s.vocab, seed=1000), name + " (sequence)", runner=run_gpu_sequence)
+
+
+def test_sequence_api_tiny_fp32():
+    s = SHAPES["tiny"]
+    check(s, sequence_tokens(s), "tiny fp32 (sequence)", runner=run_gpu_sequence)
 
 
 def test_eta0_matches_frozen_forward():
