@@ -336,18 +336,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const uint32_t sb = trow + (uint32_t)((j & 1) * 128 + b0);
         tmem_ldn<64>(sb, v);
       }
-      float mx = -INFINITY;
+      float m8[8];  // eight independent max chains
+#pragma unroll
+      for (int i = 0; i < 8; ++i) m8[i] = -INFINITY;
       if (full) {
 #pragma unroll
-        for (int i = 0; i < 64; ++i) mx = fmaxf(mx, v[i]);
+        for (int i = 0; i < 64; ++i) m8[i & 7] = fmaxf(m8[i & 7], v[i]);
       } else {
 #pragma unroll
         for (int i = 0; i < 64; ++i) {
           const bool valid = (b0 + i >= c_lo) && (b0 + i <= c_hi);
           v[i] = valid ? v[i] : -INFINITY;
-          mx = fmaxf(mx, v[i]);
+          m8[i & 7] = fmaxf(m8[i & 7], v[i]);
         }
       }
+      const float mx =
+          fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       float mo;
       if (!exchange(mx, j, mo)) {
         ok = false;
@@ -364,7 +368,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       const int pb = j % C::NP;
       uint8_t* pbuf = smem + C::P_OFF + pb * C::NOP * C::PB + hf * 16384 + r * 128;
-      float rs = 0.f;
+      float r4[4] = {0.f, 0.f, 0.f, 0.f};  // independent sum chains
 #pragma unroll
       for (int u = 0; u < 8; ++u) {  // 8 x 16-B chunks: columns b0 + 8u .. b0 + 8u + 7 (128-B swizzle)
         uint32_t hw[4], lw[4];
@@ -372,7 +376,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int e = 0; e < 4; ++e) {
           const float x0 = ex2_approx(fmaf(v[8 * u + 2 * e], sl2, -m_use));
           const float x1 = ex2_approx(fmaf(v[8 * u + 2 * e + 1], sl2, -m_use));
-          rs += x0 + x1;
+          r4[e] += x0 + x1;
           __nv_bfloat162 t = __floats2bfloat162_rn(x0, x1);
           hw[e] = *reinterpret_cast<uint32_t*>(&t);
           if (SPLIT) {
@@ -387,6 +391,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       fence_proxy_async();
       tc_fence_before();
       mbar_arrive(&p_full[pb]);
+      const float rs = (r4[0] + r4[1]) + (r4[2] + r4[3]);
       l_run = l_run * alpha + rs;
       if (C::NP == 2 && j > 0) {
         if (!accumulate(j - 1, alpha)) {
@@ -452,7 +457,16 @@ int attn_fwd_run(const AttnMaps& m, const AttnArgs& a, bool split, cudaStream_t 
     }
     return (int)cudaErrorInvalidValue;
   }
-  return attn_fwd2_run(m, a, st);  // bf16 operands: the two-tile kernel
+  // bf16 operands: the two-query-tile kernel when its grid makes two full waves, else
+  // 128-query CTAs (measured faster at one to two waves of the two-tile grid)
+  if ((long)((a.n + 255) / 256) * a.H >= 2L * num_sms()) return attn_fwd2_run(m, a, st);
+  switch (a.dh) {
+    case 32: return launch_fwd<32, false>(m, a, st);
+    case 64: return launch_fwd<64, false>(m, a, st);
+    case 96: return launch_fwd<96, false>(m, a, st);
+    case 128: return launch_fwd<128, false>(m, a, st);
+  }
+  return (int)cudaErrorInvalidValue;
 }
 
 }  // namespace ttt

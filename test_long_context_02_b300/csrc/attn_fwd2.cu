@@ -258,19 +258,23 @@ __global__ void __launch_bounds__(kF2Threads, 1)
         break;
       }
       tc_fence_after();
-      // pass 1: row max over the tile (S re-read from TMEM in pass 2 keeps registers low)
-      float mx = -INFINITY;
+      // pass 1: row max over the tile, eight independent chains (S is re-read in pass 2
+      // rather than held, which keeps registers below the 320-thread limit)
+      float mx;
+      {
+        float t[128];
+        tmem_ld128(sS, t);
+        float m8[8];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float t[32];
-        tmem_ld32(sS + (uint32_t)(c * 32), t);
+        for (int e = 0; e < 8; ++e) m8[e] = -INFINITY;
         if (full) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, t[e]);
+          for (int e = 0; e < 128; ++e) m8[e & 7] = fmaxf(m8[e & 7], t[e]);
         } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, (32 * c + e >= c_lo && 32 * c + e <= c_hi) ? t[e] : -INFINITY);
+          for (int e = 0; e < 128; ++e) m8[e & 7] = fmaxf(m8[e & 7], (e >= c_lo && e <= c_hi) ? t[e] : -INFINITY);
         }
+        mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       }
       const float m_tile = mx * sl2;
       // lazy max: move it only when the tile's max exceeds it by more than 2^8
@@ -293,7 +297,9 @@ __global__ void __launch_bounds__(kF2Threads, 1)
       }
       if (grow) m_used = m_tile;
       const float m_use = (m_used == -INFINITY) ? 0.f : m_used;
-      float rs = 0.f;
+      float r8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) r8[e] = 0.f;
       // pass 2: P as bf16 pairs written over the first 64 columns of S_i.  Chunk c
       // reads S columns 32c.. before it writes P columns 16c.., which only overlap
       // S columns already read (16c + 16 <= 32c for c >= 1; c = 0 reads first).
@@ -312,11 +318,13 @@ __global__ void __launch_bounds__(kF2Threads, 1)
           }
           const float x0 = ex2_approx(fmaf(y0, sl2, -m_use));
           const float x1 = ex2_approx(fmaf(y1, sl2, -m_use));
-          rs += x0 + x1;
+          r8[(2 * e) & 7] += x0;
+          r8[(2 * e + 1) & 7] += x1;
           u[e] = pack_bf16(x0, x1);
         }
         tmem_st16(sS + (uint32_t)(c * 16), u);
       }
+      const float rs = ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&p_full[i]);
