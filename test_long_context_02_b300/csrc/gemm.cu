@@ -56,9 +56,19 @@ TTT_DEV bool wait_drain(uint64_t* bar, uint32_t parity, int* err) {
   return true;
 }
 
-TTT_DEV float gelu_f(float a) { return 0.5f * a * (1.f + tanhf(kGeluC * (a + 0.044715f * a * a * a))); }
-TTT_DEV float gelu_grad_f(float a) {
-  const float t = tanhf(kGeluC * (a + 0.044715f * a * a * a));
+// tanh: the documented tanh.approx.f32 (about 2^-11 relative) when the result is
+// rounded to one bf16, tanhf when a bf16 remainder keeps ~2^-17 of it.
+TTT_DEV float tanh_sel(float u, bool exact) {
+  if (exact) return tanhf(u);
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(u));
+  return y;
+}
+TTT_DEV float gelu_f(float a, bool exact) {
+  return 0.5f * a * (1.f + tanh_sel(kGeluC * (a + 0.044715f * a * a * a), exact));
+}
+TTT_DEV float gelu_grad_f(float a, bool exact) {
+  const float t = tanh_sel(kGeluC * (a + 0.044715f * a * a * a), exact);
   return 0.5f * (1.f + t) + 0.5f * a * (1.f - t * t) * kGeluC * (1.f + 3.f * 0.044715f * a * a);
 }
 
@@ -104,8 +114,10 @@ TTT_DEV void store_opnd32(bf16* hi, bf16* lo, long base, const float (&v)[32], i
 #pragma unroll
       for (int i = 0; i < 4; ++i) pl[i] = make_uint4(l[4 * i], l[4 * i + 1], l[4 * i + 2], l[4 * i + 3]);
     }
-  } else {
-    for (int i = 0; i < ncols; ++i) store_opnd(hi, lo, base + i, v[i]);
+  } else {  // ragged edge: predicated, fully unrolled (v stays in registers)
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < ncols) store_opnd(hi, lo, base + i, v[i]);
   }
 }
 
@@ -135,7 +147,9 @@ TTT_DEV void store_f32_32(float* p, const float (&v)[32], int ncols) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) q[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
   } else {
-    for (int i = 0; i < ncols; ++i) p[i] = v[i];
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < ncols) p[i] = v[i];
   }
 }
 
@@ -148,7 +162,9 @@ TTT_DEV void red_add_f32_32(float* p, const float (&v)[32], int ncols) {
                    "f"(v[4 * i + 2]), "f"(v[4 * i + 3])
                    : "memory");
   } else {
-    for (int i = 0; i < ncols; ++i) atomicAdd(p + i, v[i]);
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < ncols) atomicAdd(p + i, v[i]);
   }
 }
 
@@ -161,12 +177,15 @@ TTT_DEV void load_f32_32(const float* p, float (&v)[32], int ncols) {
       v[4 * i] = t.x; v[4 * i + 1] = t.y; v[4 * i + 2] = t.z; v[4 * i + 3] = t.w;
     }
   } else {
-    for (int i = 0; i < ncols; ++i) v[i] = p[i];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = i < ncols ? p[i] : 0.f;
   }
 }
 
+constexpr int kGemmThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue (two per TMEM lane quadrant)
+
 template <int BN, bool SPLIT, int EPI, int DH>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tAl,
                 const __grid_constant__ CUtensorMap tB, const __grid_constant__ CUtensorMap tBl, const GemmArgs g) {
   using C = Cfg<BN, SPLIT>;
@@ -195,7 +214,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 128);
+      mbar_init(&tempty[b], 256);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -299,7 +318,9 @@ __global__ void __launch_bounds__(192, 1)
       wait_drain(drain, 0, g.err);
     }
   } else {  // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int q = warp & 3;             // TMEM lane quadrant this warp may access
+    const int half = (warp - 2) >> 2;   // the two warps of a quadrant take alternate column chunks
+    const bool exact = g.ol != nullptr; // bf16 remainders are kept: full-precision transcendentals
     int it = 0;
     for (int u = blockIdx.x; u < nunits; u += gridDim.x, ++it) {
       const int t = u % ntiles;
@@ -330,7 +351,7 @@ __global__ void __launch_bounds__(192, 1)
         bf16* oh = sec == 0 ? g.rq_h : (sec == 1 ? g.rk_h : g.rv_h);
         bf16* ol = sec == 0 ? g.rq_l : (sec == 1 ? g.rk_l : g.rv_l);
 #pragma unroll 1
-        for (int hh = 0; hh < BN / DH; ++hh) {
+        for (int hh = half; hh < BN / DH; hh += 2) {
           float v[DH];
 #pragma unroll
           for (int c = 0; c < DH / 32; ++c) {
@@ -359,12 +380,31 @@ __global__ void __launch_bounds__(192, 1)
           store_opnd_n<DH>(oh, ol, (long)row * g.rd + scol + hh * DH, v);
         }
       } else {
+      // Global operand of the epilogue (residual, GELU argument, fp32 weights), fetched
+      // one chunk ahead so that its latency overlaps the current chunk's work.
+      constexpr bool kLoads = EPI == EPI_RESID || EPI == EPI_GELU_BWD || EPI == EPI_SGD;
+      const float* gsrc = EPI == EPI_RESID ? g.resid : (EPI == EPI_GELU_BWD ? g.aux : g.w32);
+      const long gld = EPI == EPI_RESID ? g.ldr : (EPI == EPI_GELU_BWD ? g.ldaux : g.ldw);
+      const bool do_loads = kLoads && !(EPI == EPI_RESID && ks > 1);
+      float nxt[32];
+      if (do_loads && rok && n0 + half * 32 < g.N)
+        load_f32_32(gsrc + (long)row * gld + n0 + half * 32, nxt, min(32, g.N - n0 - half * 32));
+      // CE_FWD keeps one running (max, sum) per row: the first warp of each quadrant does all chunks
+      const int c_first = EPI == EPI_CE_FWD ? 0 : half;
+      const int c_step = EPI == EPI_CE_FWD ? 1 : 2;
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = c_first; c < BN / 32 && !(EPI == EPI_CE_FWD && half); c += c_step) {
         float v[32];
         tmem_ld32(taddr + (uint32_t)(c * 32), v);
         const int c0 = n0 + c * 32;
         const int ncols = min(32, g.N - c0);
+        float cur[32];
+        if (do_loads) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) cur[i] = nxt[i];
+          const int cn = n0 + (c + 2) * 32;
+          if (rok && c + 2 < BN / 32 && cn < g.N) load_f32_32(gsrc + (long)row * gld + cn, nxt, min(32, g.N - cn));
+        }
         if (!rok || ncols <= 0) continue;
         if ((EPI == EPI_F32 || EPI == EPI_RESID) && ks > 1) {
           // K slice: add the partial sum (out32 holds 0, or the residual, before the first slice lands)
@@ -374,30 +414,24 @@ __global__ void __launch_bounds__(192, 1)
         } else if (EPI == EPI_OPND) {
           store_opnd32(g.oh, g.ol, (long)row * g.ldo + c0, v, ncols);
         } else if (EPI == EPI_RESID) {
-          float r[32];
-          load_f32_32(g.resid + (long)row * g.ldr + c0, r, ncols);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] += v[i];
-          store_f32_32(g.out32 + (long)row * g.ldo32 + c0, r, ncols);
+          for (int i = 0; i < 32; ++i) cur[i] += v[i];
+          store_f32_32(g.out32 + (long)row * g.ldo32 + c0, cur, ncols);
         } else if (EPI == EPI_GELU) {
           if (g.out32) store_f32_32(g.out32 + (long)row * g.ldo32 + c0, v, ncols);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = gelu_f(v[i]);
+          for (int i = 0; i < 32; ++i) v[i] = gelu_f(v[i], exact);
           store_opnd32(g.oh, g.ol, (long)row * g.ldo + c0, v, ncols);
         } else if (EPI == EPI_GELU_BWD) {
-          float a[32];
-          load_f32_32(g.aux + (long)row * g.ldaux + c0, a, ncols);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] *= gelu_grad_f(a[i]);
+          for (int i = 0; i < 32; ++i) v[i] *= gelu_grad_f(cur[i], exact);
           store_opnd32(g.oh, g.ol, (long)row * g.ldo + c0, v, ncols);
         } else if (EPI == EPI_SGD) {
-          float w[32];
           float* wp = g.w32 + (long)row * g.ldw + c0;
-          load_f32_32(wp, w, ncols);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) w[i] -= g.eta * v[i];
-          store_f32_32(wp, w, ncols);
-          store_opnd32(g.wh, g.wl, (long)row * g.ldw + c0, w, ncols);
+          for (int i = 0; i < 32; ++i) cur[i] -= g.eta * v[i];
+          store_f32_32(wp, cur, ncols);
+          store_opnd32(g.wh, g.wl, (long)row * g.ldw + c0, cur, ncols);
         } else if (EPI == EPI_CE_FWD) {
           float mx = -INFINITY;
 #pragma unroll
@@ -423,7 +457,7 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
       }
-      if (EPI == EPI_CE_FWD && rok) g.part[(long)ntile * g.M + row] = make_float2(ce_m, ce_s);
+      if (EPI == EPI_CE_FWD && rok && half == 0) g.part[(long)ntile * g.M + row] = make_float2(ce_m, ce_s);
       tc_fence_before();
       mbar_arrive(&tempty[buf]);
     }
@@ -457,7 +491,7 @@ int launch(const CUtensorMap& a, const CUtensorMap& al, const CUtensorMap& b, co
   }
   const int tiles = ((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN) * (g.ksplit > 1 ? g.ksplit : 1);
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  kern<<<grid, 192, C::SMEM, st>>>(a, al, b, bl, g);
+  kern<<<grid, kGemmThreads, C::SMEM, st>>>(a, al, b, bl, g);
   return (int)cudaGetLastError();
 }
 
@@ -485,7 +519,9 @@ int pick_bn(int M, int N) {
   const int sms = num_sms();
   const int mt = (M + BM - 1) / BM;
   const long t256 = (long)mt * ((N + 255) / 256), t128 = (long)mt * ((N + 127) / 128);
-  const long c256 = ((t256 + sms - 1) / sms) * 256, c128 = ((t128 + sms - 1) / sms) * 128;
+  // waves x tile width, the 128-wide tile weighted by its lower MMA rate per byte of
+  // shared memory (measured ~0.6 of the 256-wide tile on the same product)
+  const double c256 = (double)((t256 + sms - 1) / sms) * 256, c128 = (double)((t128 + sms - 1) / sms) * 128 * 1.6;
   return (N <= 128 || c128 < c256) ? 128 : 256;
 }
 
@@ -542,14 +578,15 @@ int gemm_qkv_rope(const Opnd& A, const Opnd& B, GemmArgs g, int dh, bool split, 
 void choose_tiling(int M, int N, int K, bool allow_slices, int* bn_out, int* ks_out) {
   const long sms = num_sms();
   const long mt = (M + BM - 1) / BM, nk = (K + BK - 1) / BK;
-  long best = -1;
+  double best = -1;
   for (int bn : {256, 128}) {
     if (bn == 256 && N <= 128) continue;
     const long tiles = mt * ((N + bn - 1) / bn);
     for (int ks = 1; ks <= (allow_slices ? 8 : 1); ++ks) {
       if (ks > 1 && (tiles >= sms || nk / ks < 4)) break;
       const long units = tiles * ks;
-      const long cost = ((units + sms - 1) / sms) * bn * ((nk + ks - 1) / ks) + 2 * ks;  // + slice overhead
+      const double cost = (double)((units + sms - 1) / sms) * bn * (bn == 128 ? 1.6 : 1.0) * ((nk + ks - 1) / ks) +
+                          2 * ks;  // + slice overhead; the 128-wide tile weighted as in pick_bn
       if (best < 0 || cost < best) {
         best = cost;
         *bn_out = bn;
