@@ -450,6 +450,14 @@ int launch_fwd(const AttnMaps& m, const AttnArgs& a, cudaStream_t st) {
 
 int attn_fwd_run(const AttnMaps& m, const AttnArgs& a, bool split, cudaStream_t st) {
   if (a.n <= 0) return 0;
+  // bf16 operands: the two-query-tile kernel when its grid makes two full waves
+  if (!split && (long)((a.n + 255) / 256) * a.H >= 2L * num_sms()) return attn_fwd2_run(m, a, st);
+  return attn_fwd3_run(m, a, split, st);
+}
+
+// The earlier one-tile kernel (P through shared memory, O in registers).
+int attn_fwd1_run(const AttnMaps& m, const AttnArgs& a, bool split, cudaStream_t st) {
+  if (a.n <= 0) return 0;
   if (split) {
     switch (a.dh) {
       case 32: return launch_fwd<32, true>(m, a, st);
@@ -457,9 +465,6 @@ int attn_fwd_run(const AttnMaps& m, const AttnArgs& a, bool split, cudaStream_t 
     }
     return (int)cudaErrorInvalidValue;
   }
-  // bf16 operands: the two-query-tile kernel when its grid makes two full waves, else
-  // 128-query CTAs (measured faster at one to two waves of the two-tile grid)
-  if ((long)((a.n + 255) / 256) * a.H >= 2L * num_sms()) return attn_fwd2_run(m, a, st);
   switch (a.dh) {
     case 32: return launch_fwd<32, false>(m, a, st);
     case 64: return launch_fwd<64, false>(m, a, st);
