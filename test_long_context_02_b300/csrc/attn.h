@@ -48,5 +48,9 @@ struct AttnBwdMaps {
 
 // which: 0 = both kernels, 1 = dQ only, 2 = dK/dV only
 int attn_bwd_run(const AttnBwdMaps& m, const AttnBwdArgs& a, bool split, cudaStream_t st, int which = 0);
+// dQ with dS kept in TMEM (attn_dq2.cu); dK/dV with P^T, dS^T kept in TMEM (attn_dkv2.cu).
+int attn_dq2_run(const AttnBwdMaps& m, const AttnBwdArgs& a, bool split, cudaStream_t st);
+int attn_dkv2_run(const AttnBwdMaps& m, const AttnBwdArgs& a, bool split, cudaStream_t st);
+int attn_bwd1_run(const AttnBwdMaps& m, const AttnBwdArgs& a, bool split, cudaStream_t st, int which);
 
 }  // namespace ttt

@@ -598,6 +598,16 @@ int launch_bwd(const AttnBwdMaps& m, const AttnBwdArgs& a, cudaStream_t st, int 
 
 int attn_bwd_run(const AttnBwdMaps& m, const AttnBwdArgs& a, bool split, cudaStream_t st, int which) {
   if (a.g.n <= 0) return 0;
+  if (which != 2) {
+    const int r = attn_dq2_run(m, a, split, st);
+    if (r != 0) return r;
+  }
+  return which != 1 ? attn_dkv2_run(m, a, split, st) : 0;
+}
+
+// The earlier kernels (dS and P^T through shared memory).
+int attn_bwd1_run(const AttnBwdMaps& m, const AttnBwdArgs& a, bool split, cudaStream_t st, int which) {
+  if (a.g.n <= 0) return 0;
   if (split) {
     switch (a.g.dh) {
       case 32: return launch_bwd<32, true>(m, a, st, which);
