@@ -27,7 +27,6 @@ struct AttnMaps {
 int attn_fwd_run(const AttnMaps& m, const AttnArgs& a, bool split, cudaStream_t st);
 // bf16 operands only: two query tiles per CTA, P kept in TMEM (attn_fwd2.cu).
 int attn_fwd2_run(const AttnMaps& m, const AttnArgs& a, cudaStream_t st);
-int attn_fwd1_run(const AttnMaps& m, const AttnArgs& a, bool split, cudaStream_t st);
 // One query tile per CTA, P and O kept in TMEM (attn_fwd3.cu).
 int attn_fwd3_run(const AttnMaps& m, const AttnArgs& a, bool split, cudaStream_t st);
 
@@ -51,6 +50,6 @@ int attn_bwd_run(const AttnBwdMaps& m, const AttnBwdArgs& a, bool split, cudaStr
 // dQ with dS kept in TMEM (attn_dq2.cu); dK/dV with P^T, dS^T kept in TMEM (attn_dkv2.cu).
 int attn_dq2_run(const AttnBwdMaps& m, const AttnBwdArgs& a, bool split, cudaStream_t st);
 int attn_dkv2_run(const AttnBwdMaps& m, const AttnBwdArgs& a, bool split, cudaStream_t st);
-int attn_bwd1_run(const AttnBwdMaps& m, const AttnBwdArgs& a, bool split, cudaStream_t st, int which);
+
 
 }  // namespace ttt

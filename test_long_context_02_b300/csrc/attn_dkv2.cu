@@ -148,6 +148,8 @@ __global__ void __launch_bounds__(kK2Threads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // the predecessor kernel's outputs are complete and visible from here on
+  pdl_launch_dependents();
   const uint32_t T_S = 0, T_DP = 128, T_DV = 256, T_DK = 256 + C::DP;
 
   if (warp == 0) {  // ---------------------------------------------- TMA producer + statistics
@@ -339,8 +341,7 @@ int launch_dkv2(const AttnBwdMaps& m, const AttnBwdArgs& a, cudaStream_t st) {
   }
   dim3 grid((a.g.n + 127) / 128, a.g.H);
   const AttnMaps& f = m.f;
-  kern<<<grid, kK2Threads, C::SMEM, st>>>(f.q, f.ql, m.dO, m.dOl, f.ko, f.kol, f.vo, f.vol, a);
-  return (int)cudaGetLastError();
+  return (int)launch_k(kern, grid, dim3(kK2Threads), C::SMEM, st, f.q, f.ql, m.dO, m.dOl, f.ko, f.kol, f.vo, f.vol, a);
 }
 
 }  // namespace

@@ -149,6 +149,8 @@ __global__ void __launch_bounds__(kQ2Threads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // the predecessor kernel's outputs are complete and visible from here on
+  pdl_launch_dependents();
   const uint32_t T_DP = 256, T_DQ = 384;  // score buffers at 0 and 128
 
   auto tile_row0 = [&](int j, bool& own) -> int {
@@ -337,9 +339,8 @@ int launch_dq2(const AttnBwdMaps& m, const AttnBwdArgs& a, cudaStream_t st) {
   }
   dim3 grid((a.g.n + 127) / 128, a.g.H);
   const AttnMaps& f = m.f;
-  kern<<<grid, kQ2Threads, C::SMEM, st>>>(f.q, f.ql, m.dO, m.dOl, f.kr, f.krl, f.vr, f.vrl, f.ko, f.kol, f.vo, f.vol,
-                                           a);
-  return (int)cudaGetLastError();
+  return (int)launch_k(kern, grid, dim3(kQ2Threads), C::SMEM, st, f.q, f.ql, m.dO, m.dOl, f.kr, f.krl, f.vr, f.vrl,
+                       f.ko, f.kol, f.vo, f.vol, a);
 }
 
 }  // namespace

@@ -131,6 +131,8 @@ __global__ void __launch_bounds__(kF2Threads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;  // S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512)
+  pdl_wait();  // the predecessor kernel's outputs are complete and visible from here on
+  pdl_launch_dependents();
 
   auto tile_row0 = [&](int j, bool& own) -> int {
     if (j < tr.n_ring) {
@@ -371,8 +373,7 @@ int launch_fwd2(const AttnMaps& m, const AttnArgs& a, cudaStream_t st) {
     attr = true;
   }
   dim3 grid((a.n + 255) / 256, a.H);
-  kern<<<grid, kF2Threads, C::SMEM, st>>>(m.q, m.kr, m.vr, m.ko, m.vo, a);
-  return (int)cudaGetLastError();
+  return (int)launch_k(kern, grid, dim3(kF2Threads), C::SMEM, st, m.q, m.kr, m.vr, m.ko, m.vo, a);
 }
 
 }  // namespace

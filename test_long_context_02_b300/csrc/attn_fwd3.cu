@@ -173,6 +173,8 @@ __global__ void __launch_bounds__(kF3Threads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;  // S buffers [0,128) and [128,256); O [256, 256 + DH)
+  pdl_wait();  // the predecessor kernel's outputs are complete and visible from here on
+  pdl_launch_dependents();
 
   auto tile_row0 = [&](int j, bool& own) -> int {
     if (j < tr.n_ring) {
@@ -432,8 +434,8 @@ int launch_fwd3(const AttnMaps& m, const AttnArgs& a, cudaStream_t st) {
     attr = true;
   }
   dim3 grid((a.n + 127) / 128, a.H);
-  kern<<<grid, kF3Threads, C::SMEM, st>>>(m.q, m.ql, m.kr, m.krl, m.vr, m.vrl, m.ko, m.kol, m.vo, m.vol, a);
-  return (int)cudaGetLastError();
+  return (int)launch_k(kern, grid, dim3(kF3Threads), C::SMEM, st, m.q, m.ql, m.kr, m.krl, m.vr, m.vrl, m.ko, m.kol,
+                       m.vo, m.vol, a);
 }
 
 }  // namespace

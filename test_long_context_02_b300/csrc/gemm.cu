@@ -234,6 +234,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // the predecessor kernel's outputs are complete and visible from here on
+  pdl_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) {  // ---------------------------------------------- TMA producer
@@ -491,8 +493,7 @@ int launch(const CUtensorMap& a, const CUtensorMap& al, const CUtensorMap& b, co
   }
   const int tiles = ((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN) * (g.ksplit > 1 ? g.ksplit : 1);
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  kern<<<grid, kGemmThreads, C::SMEM, st>>>(a, al, b, bl, g);
-  return (int)cudaGetLastError();
+  return (int)launch_k(kern, dim3(grid), dim3(kGemmThreads), C::SMEM, st, a, al, b, bl, g);
 }
 
 template <int BN, bool SPLIT>

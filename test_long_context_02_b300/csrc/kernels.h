@@ -8,6 +8,24 @@ namespace ttt {
 
 using bf16 = __nv_bfloat16;
 
+// Launch with programmatic stream serialisation: the kernel may begin while
+// its predecessor drains (every kernel here calls pdl_wait() before touching
+// global memory).  Returns the launch's cudaError_t.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // ------------------------------------------------------------------ GEMM
 // C[M,N] = A[M,K] . B[N,K]^T on tcgen05 (bf16 operands, fp32 accumulate in
 // TMEM), followed by one of these epilogues on each fp32 accumulator value.

@@ -83,6 +83,15 @@ TTT_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
   }
 }
 
+// ------------------------------------------------ programmatic dependent launch
+// Kernels are launched with programmatic stream serialisation, so a kernel may
+// start (and run its prologue) while its predecessor on the stream finishes.
+// pdl_wait() blocks until every predecessor grid has completed and its memory
+// writes are visible; it comes before the kernel's first global-memory access.
+// pdl_launch_dependents() lets the next kernel start launching.
+TTT_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+TTT_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // --------------------------------------------------------------------- TMA
 TTT_DEV void tma_prefetch(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

@@ -66,6 +66,8 @@ TTT_DEV void load8_bf(const bf16* hi, const bf16* lo, long off, float (&v)[8]) {
 // x[t][:] = E[tok[t]][:]; bad ids are reported and read row 0.
 __global__ void embed_kernel(const int* __restrict__ tok, int n, const float* __restrict__ E, int V, int d,
                              float* __restrict__ x, int* err) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (row >= n) return;
   int id = tok[row];
@@ -81,6 +83,8 @@ __global__ void embed_kernel(const int* __restrict__ tok, int n, const float* __
 // Next-token targets of the chunk: tgt[i] = tok[i+1] (i < n-1), tgt[n-1] = *next (-1: none).
 __global__ void targets_kernel(const int* __restrict__ tok, int n, const int* __restrict__ next, int V,
                                int* __restrict__ tgt, int* err) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
   int t = (i + 1 < n) ? tok[i + 1] : *next;
@@ -98,6 +102,8 @@ template <int NCH>
 __global__ void __launch_bounds__(128) rmsnorm_kernel(const float* __restrict__ x, const float* __restrict__ g,
                                                       float eps, int n, int d, bf16* __restrict__ yh,
                                                       bf16* __restrict__ yl, float* __restrict__ rstd) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (row >= n) return;
   const float* xr = x + (long)row * d;
@@ -135,6 +141,8 @@ __global__ void __launch_bounds__(128) rmsnorm_bwd_kernel(const float* __restric
                                                           const float* __restrict__ g, const float* __restrict__ rstd,
                                                           const float* resid, int n, int d, float* out,
                                                           bf16* __restrict__ oh, bf16* __restrict__ ol) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (row >= n) return;
   const long base = (long)row * d;
@@ -180,6 +188,8 @@ __global__ void __launch_bounds__(128) rmsnorm_bwd_kernel(const float* __restric
 // cos/sin of pos * theta^(-2i/dh) for the chunk, angles formed and reduced in fp64.
 __global__ void rope_table_kernel(long pos0, int n, int half, const double* __restrict__ inv_freq,
                                   float* __restrict__ cs, float* __restrict__ sn) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= n * half) return;
   const int t = idx / half, i = idx % half;
@@ -194,6 +204,8 @@ __global__ void rope_table_kernel(long pos0, int n, int half, const double* __re
 __global__ void rope_qkv_kernel(const float* __restrict__ qkv, const float* __restrict__ cs,
                                 const float* __restrict__ sn, int n, int H, int dh, bf16* qh, bf16* ql, bf16* kh,
                                 bf16* kl, bf16* vh, bf16* vl) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int half = dh / 2, groups = half / 4;
   const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= (long)n * H * groups) return;
@@ -250,6 +262,8 @@ __global__ void rope_qkv_kernel(const float* __restrict__ qkv, const float* __re
 __global__ void rope_bwd_kernel(const float* __restrict__ dq, const float* __restrict__ dk,
                                 const float* __restrict__ dv, const float* __restrict__ cs,
                                 const float* __restrict__ sn, int n, int H, int dh, bf16* oh, bf16* ol) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int half = dh / 2;
   const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= (long)n * H * half) return;
@@ -276,6 +290,8 @@ __global__ void rope_bwd_kernel(const float* __restrict__ dq, const float* __res
 // grid = (tokens, layers)
 __global__ void commit_kernel(const bf16* __restrict__ own, bf16* __restrict__ ring, long own_layer_stride,
                               long ring_layer_stride, long pos0, int n, int window, int d) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int t = blockIdx.x;
   const int l = blockIdx.y;
   if (t >= n) return;
@@ -289,6 +305,8 @@ __global__ void commit_kernel(const bf16* __restrict__ own, bf16* __restrict__ r
 __global__ void ce_combine_kernel(const float2* __restrict__ part, const float* __restrict__ zt,
                                   const int* __restrict__ tgt, int n, int ntiles, float* __restrict__ lse,
                                   float* __restrict__ loss_row) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int r = blockIdx.x * blockDim.x + threadIdx.x;
   if (r >= n) return;
   float m = -INFINITY;
@@ -306,6 +324,8 @@ __global__ void ce_combine_kernel(const float2* __restrict__ part, const float* 
 // Mean over the rows with a target, fixed reduction order (bit-reproducible).
 __global__ void loss_mean_kernel(const float* __restrict__ loss_row, const int* __restrict__ tgt, int n,
                                  float* __restrict__ out, float* __restrict__ inv_count) {
+  pdl_wait();
+  pdl_launch_dependents();
   __shared__ float ssum[32];
   __shared__ int scnt[32];
   float s = 0.f;
@@ -339,6 +359,8 @@ __global__ void loss_mean_kernel(const float* __restrict__ loss_row, const int* 
 __global__ void attn_rowdot_kernel(const bf16* __restrict__ doh, const bf16* __restrict__ dol,
                                    const bf16* __restrict__ oh, const bf16* __restrict__ ol, int n, int H,
                                    int dh, float* __restrict__ D) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (w >= n * H) return;
   const int t = w / H, h = w % H;
@@ -358,6 +380,8 @@ __global__ void attn_rowdot_kernel(const bf16* __restrict__ doh, const bf16* __r
 // dst[r][c] = split(src[r][c]) for r < rows, c < cols (weight upload / layout change).
 __global__ void convert_kernel(const float* __restrict__ src, long rows, int cols, long src_ld, bf16* dh, bf16* dl,
                                long dst_ld) {
+  pdl_wait();
+  pdl_launch_dependents();
   const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= rows * cols) return;
   const long r = idx / cols;
@@ -374,13 +398,11 @@ inline int row_grid(int n) { return (n + kRowWarps - 1) / kRowWarps; }
 }  // namespace
 
 int rows_embed(const int* tok, int n, const float* E, int V, int d, float* x, int* err, cudaStream_t st) {
-  embed_kernel<<<row_grid(n), kRowWarps * 32, 0, st>>>(tok, n, E, V, d, x, err);
-  return (int)cudaGetLastError();
+  return (int)launch_k(embed_kernel, dim3(row_grid(n)), dim3(kRowWarps * 32), 0, st, tok, n, E, V, d, x, err);
 }
 
 int rows_targets(const int* tok, int n, const int* next, int V, int* tgt, int* err, cudaStream_t st) {
-  targets_kernel<<<(n + 255) / 256, 256, 0, st>>>(tok, n, next, V, tgt, err);
-  return (int)cudaGetLastError();
+  return (int)launch_k(targets_kernel, dim3((n + 255) / 256), dim3(256), 0, st, tok, n, next, V, tgt, err);
 }
 
 // Row kernels of the norm: 4 warps (4 rows) per block, per-lane register chunks
@@ -395,8 +417,7 @@ int norm_fwd_n(const float* x, const float* g, float eps, int n, int d, bf16* yh
     return (int)cudaErrorInvalidValue;
   } else {
     if ((d + 255) / 256 > NCH) return norm_fwd_n<NCH + 1>(x, g, eps, n, d, yh, yl, rstd, st);
-    rmsnorm_kernel<NCH><<<(n + kNormWarps - 1) / kNormWarps, kNormWarps * 32, 0, st>>>(x, g, eps, n, d, yh, yl, rstd);
-    return (int)cudaGetLastError();
+    return (int)launch_k(rmsnorm_kernel<NCH>, dim3((n + kNormWarps - 1) / kNormWarps), dim3(kNormWarps * 32), 0, st, x, g, eps, n, d, yh, yl, rstd);
   }
 }
 
@@ -407,9 +428,7 @@ int norm_bwd_n(const float* dy, const float* x, const float* g, const float* rst
     return (int)cudaErrorInvalidValue;
   } else {
     if ((d + 255) / 256 > NCH) return norm_bwd_n<NCH + 1>(dy, x, g, rstd, resid, n, d, out, oh, ol, st);
-    rmsnorm_bwd_kernel<NCH><<<(n + kNormWarps - 1) / kNormWarps, kNormWarps * 32, 0, st>>>(dy, x, g, rstd, resid, n,
-                                                                                           d, out, oh, ol);
-    return (int)cudaGetLastError();
+    return (int)launch_k(rmsnorm_bwd_kernel<NCH>, dim3((n + kNormWarps - 1) / kNormWarps), dim3(kNormWarps * 32), 0, st, dy, x, g, rstd, resid, n, d, out, oh, ol);
   }
 }
 
@@ -429,56 +448,48 @@ int rows_rmsnorm_bwd(const float* dy, const float* x, const float* g, const floa
 
 int rows_rope_table(long pos0, int n, int dh, const double* inv_freq, float* cs, float* sn, cudaStream_t st) {
   const int half = dh / 2, tot = n * half;
-  rope_table_kernel<<<(tot + 255) / 256, 256, 0, st>>>(pos0, n, half, inv_freq, cs, sn);
-  return (int)cudaGetLastError();
+  return (int)launch_k(rope_table_kernel, dim3((tot + 255) / 256), dim3(256), 0, st, pos0, n, half, inv_freq, cs, sn);
 }
 
 int rows_rope_qkv(const float* qkv, const float* cs, const float* sn, int n, int H, int dh, bf16* qh, bf16* ql,
                   bf16* kh, bf16* kl, bf16* vh, bf16* vl, cudaStream_t st) {
   const long tot = (long)n * H * (dh / 8);
-  rope_qkv_kernel<<<(unsigned)((tot + 255) / 256), 256, 0, st>>>(qkv, cs, sn, n, H, dh, qh, ql, kh, kl, vh, vl);
-  return (int)cudaGetLastError();
+  return (int)launch_k(rope_qkv_kernel, dim3((unsigned)((tot + 255) / 256)), dim3(256), 0, st, qkv, cs, sn, n, H, dh, qh, ql, kh, kl, vh, vl);
 }
 
 int rows_rope_bwd(const float* dq, const float* dk, const float* dv, const float* cs, const float* sn, int n, int H,
                   int dh, bf16* oh, bf16* ol, cudaStream_t st) {
   const long tot = (long)n * H * (dh / 2);
-  rope_bwd_kernel<<<(unsigned)((tot + 255) / 256), 256, 0, st>>>(dq, dk, dv, cs, sn, n, H, dh, oh, ol);
-  return (int)cudaGetLastError();
+  return (int)launch_k(rope_bwd_kernel, dim3((unsigned)((tot + 255) / 256)), dim3(256), 0, st, dq, dk, dv, cs, sn, n, H, dh, oh, ol);
 }
 
 int rows_commit(const bf16* own, bf16* ring, long own_layer_stride, long ring_layer_stride, int n_layers, long pos0,
                 int n, int window, int d, cudaStream_t st) {
   if (n <= 0 || n_layers <= 0) return 0;
   dim3 grid(n, n_layers);
-  commit_kernel<<<grid, 128, 0, st>>>(own, ring, own_layer_stride, ring_layer_stride, pos0, n, window, d);
-  return (int)cudaGetLastError();
+  return (int)launch_k(commit_kernel, dim3(grid), dim3(128), 0, st, own, ring, own_layer_stride, ring_layer_stride, pos0, n, window, d);
 }
 
 int rows_ce_combine(const float2* part, const float* zt, const int* tgt, int n, int ntiles, float* lse,
                     float* loss_row, cudaStream_t st) {
-  ce_combine_kernel<<<(n + 127) / 128, 128, 0, st>>>(part, zt, tgt, n, ntiles, lse, loss_row);
-  return (int)cudaGetLastError();
+  return (int)launch_k(ce_combine_kernel, dim3((n + 127) / 128), dim3(128), 0, st, part, zt, tgt, n, ntiles, lse, loss_row);
 }
 
 int rows_loss_mean(const float* loss_row, const int* tgt, int n, float* out, float* inv_count, cudaStream_t st) {
-  loss_mean_kernel<<<1, 1024, 0, st>>>(loss_row, tgt, n, out, inv_count);
-  return (int)cudaGetLastError();
+  return (int)launch_k(loss_mean_kernel, dim3(1), dim3(1024), 0, st, loss_row, tgt, n, out, inv_count);
 }
 
 int rows_convert(const float* src, long rows, int cols, long src_ld, bf16* dh, bf16* dl, long dst_ld,
                  cudaStream_t st) {
   const long tot = rows * cols;
   if (tot <= 0) return 0;
-  convert_kernel<<<(unsigned)((tot + 255) / 256), 256, 0, st>>>(src, rows, cols, src_ld, dh, dl, dst_ld);
-  return (int)cudaGetLastError();
+  return (int)launch_k(convert_kernel, dim3((unsigned)((tot + 255) / 256)), dim3(256), 0, st, src, rows, cols, src_ld, dh, dl, dst_ld);
 }
 
 int rows_attn_rowdot(const bf16* doh, const bf16* dol, const bf16* oh, const bf16* ol, int n, int H, int dh, float* D,
                      cudaStream_t st) {
   const int warps = n * H;
-  attn_rowdot_kernel<<<(warps + kRowWarps - 1) / kRowWarps, kRowWarps * 32, 0, st>>>(doh, dol, oh, ol, n, H, dh, D);
-  return (int)cudaGetLastError();
+  return (int)launch_k(attn_rowdot_kernel, dim3((warps + kRowWarps - 1) / kRowWarps), dim3(kRowWarps * 32), 0, st, doh, dol, oh, ol, n, H, dh, D);
 }
 
 }  // namespace ttt
