@@ -575,7 +575,8 @@ int gemm_qkv_rope(const Opnd& A, const Opnd& B, GemmArgs g, int dh, bool split, 
 
 // Tile width and K slices for an M x N x K product: the fewest (waves x tile width x
 // k-blocks per unit) per SM, preferring the wider tile and fewer slices on ties.
-// Slices only when allowed (F32 / RESID epilogues) and each keeps >= 4 k-blocks.
+// Slices only when allowed (F32 / RESID epilogues) and each keeps >= 4 k-blocks;
+// they pay off where the tiles fill the last wave poorly.
 void choose_tiling(int M, int N, int K, bool allow_slices, int* bn_out, int* ks_out) {
   const long sms = num_sms();
   const long mt = (M + BM - 1) / BM, nk = (K + BK - 1) / BK;
@@ -584,10 +585,12 @@ void choose_tiling(int M, int N, int K, bool allow_slices, int* bn_out, int* ks_
     if (bn == 256 && N <= 128) continue;
     const long tiles = mt * ((N + bn - 1) / bn);
     for (int ks = 1; ks <= (allow_slices ? 8 : 1); ++ks) {
-      if (ks > 1 && (tiles >= sms || nk / ks < 4)) break;
+      if (ks > 1 && nk / ks < 4) break;
       const long units = tiles * ks;
-      const double cost = (double)((units + sms - 1) / sms) * bn * (bn == 128 ? 1.6 : 1.0) * ((nk + ks - 1) / ks) +
-                          2 * ks;  // + slice overhead; the 128-wide tile weighted as in pick_bn
+      // per unit: its k-blocks, plus about two k-blocks' worth for the atomic epilogue of a slice;
+      // the 128-wide tile weighted as in pick_bn
+      const double cost = (double)((units + sms - 1) / sms) * bn * (bn == 128 ? 1.6 : 1.0) *
+                          ((nk + ks - 1) / ks + (ks > 1 ? 2 : 0));
       if (best < 0 || cost < best) {
         best = cost;
         *bn_out = bn;
