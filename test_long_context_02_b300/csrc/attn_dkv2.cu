@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(kK2Threads, 1)
       const float* sl = stats + s * 256 + b0;  // this thread's 64 query columns
       const float* sd = sl + 128;
       float pv[64];
-      ld_cols_k2<64>(trow + T_S + b0, pv);  // S^T row
+      tmem_ld64(trow + T_S + b0, pv);  // S^T row
 #pragma unroll
       for (int e = 0; e < 64; ++e) {
         const float pr = ex2_approx(fmaf(pv[e], sl2, -sl[e]));

@@ -278,9 +278,10 @@ __global__ void __launch_bounds__(kQ2Threads, 1)
         break;
       }
       tc_fence_after();
-      float sv[64], dp[64];
-      ld_cols_q2<64>(trow + (uint32_t)(s * 128 + b0), sv);
-      ld_cols_q2<64>(trow + T_DP + (uint32_t)b0, dp);
+      float sd[128];  // [0,64): S row, [64,128): dP row, under one wait
+      tmem_ld64x2(trow + (uint32_t)(s * 128 + b0), trow + T_DP + (uint32_t)b0, sd);
+      const float* sv = sd;
+      const float* dp = sd + 64;
       uint32_t hi[32], lo[32];
 #pragma unroll
       for (int e = 0; e < 32; ++e) {

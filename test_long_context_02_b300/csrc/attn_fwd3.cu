@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(kF3Threads, 1)
       tc_fence_after();
       const uint32_t tS = trow + (uint32_t)(s * 128 + b0);
       float v[64];
-      ld_cols<64>(tS, v);
+      tmem_ld64(tS, v);  // one load, one wait
       float m8[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) m8[e] = -INFINITY;
