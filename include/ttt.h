@@ -129,6 +129,16 @@ TTT_API int ttt_sync(ttt_ctx* ctx);
 TTT_API int ttt_get_fast_weights(ttt_ctx* ctx, int32_t seq, int32_t suffix_layer, float* w_up, float* w_down);
 
 /*
+ * Copy the key/value window cache of block `layer` of sequence `seq` to host
+ * memory (for checks and state export): k_out, v_out float [window][d_model]
+ * (post-RoPE keys; the value of each bf16 operand, plus its remainder in the
+ * fp32 mode); pos_out int64 [window], the absolute position whose keys/values
+ * slot i holds (the latest p < position with p mod window == i), -1 if none.
+ * Any output may be NULL.  Synchronises the context stream.
+ */
+TTT_API int ttt_get_window(ttt_ctx* ctx, int32_t seq, int32_t layer, float* k_out, float* v_out, int64_t* pos_out);
+
+/*
  * Restart every sequence from the loaded weights without re-uploading them:
  * position 0, empty window cache, fast weights = the loaded W_up / W_down.
  * Enqueued on the context stream.

@@ -124,6 +124,7 @@ ttt_position = _sig("ttt_position", _i64, _vp)
 ttt_destroy = _sig("ttt_destroy", None, _vp)
 ttt_last_error = _sig("ttt_last_error", ctypes.c_char_p, _vp)
 ttt_reset = _sig("ttt_reset", ctypes.c_int, _vp)
+ttt_get_window = _sig("ttt_get_window", ctypes.c_int, _vp, _i32, _i32, _vp, _vp, _vp)
 ttt_launch_count = _sig("ttt_launch_count", _i64, _vp)
 
 
@@ -246,6 +247,16 @@ class TTT:
         self._check(ttt_get_fast_weights(self._h, seq, suffix_layer, up.ctypes.data, down.ctypes.data),
                     "ttt_get_fast_weights")
         return up, down
+
+    def window(self, seq: int, layer: int):
+        """(keys [k][d], values [k][d], positions [k]) of the window cache of one block."""
+        k, d = self.cfg.window, self.cfg.d_model
+        ko = np.zeros((k, d), np.float32)
+        vo = np.zeros((k, d), np.float32)
+        po = np.zeros(k, np.int64)
+        self._check(ttt_get_window(self._h, seq, layer, ko.ctypes.data, vo.ctypes.data, po.ctypes.data),
+                    "ttt_get_window")
+        return ko, vo, po
 
     def reset(self):
         self._check(ttt_reset(self._h), "ttt_reset")

@@ -810,6 +810,43 @@ extern "C" int ttt_get_fast_weights(ttt_ctx* c, int32_t seq, int32_t sl, float* 
   return TTT_OK;
 }
 
+extern "C" int ttt_get_window(ttt_ctx* c, int32_t seq, int32_t layer, float* k_out, float* v_out, int64_t* pos_out) {
+  if (!c || seq < 0 || seq >= c->B || layer < 0 || layer >= c->L) return TTT_ERR_ARG;
+  const long d = c->d, k = c->k;
+  const Seq& s = c->seqs[seq];
+  cudaError_t e = cudaStreamSynchronize(c->st);
+  if (e != cudaSuccess) return fail(c, TTT_ERR_CUDA, cudaGetErrorString(e));
+  if (pos_out) {  // slot i holds the latest position p < pos with p mod k == i (-1: never written)
+    for (long i = 0; i < k; ++i) {
+      long p = s.pos - 1 - ((s.pos - 1 - i) % k + k) % k;
+      pos_out[i] = (s.pos > 0 && p >= 0) ? p : -1;
+    }
+  }
+  std::vector<uint16_t> hi((size_t)k * d), lo(c->split ? (size_t)k * d : 0);
+  const Pair* rings[2] = {&s.ring_k, &s.ring_v};
+  float* outs[2] = {k_out, v_out};
+  for (int w = 0; w < 2; ++w) {
+    if (!outs[w]) continue;
+    const Pair r = rings[w]->at((long)layer * k * d);
+    e = cudaMemcpy(hi.data(), r.hi, hi.size() * 2, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && r.lo) e = cudaMemcpy(lo.data(), r.lo, lo.size() * 2, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail(c, TTT_ERR_CUDA, cudaGetErrorString(e));
+    for (size_t i = 0; i < hi.size(); ++i) {
+      uint32_t bits = (uint32_t)hi[i] << 16;
+      float v;
+      std::memcpy(&v, &bits, 4);
+      if (r.lo) {
+        uint32_t lb = (uint32_t)lo[i] << 16;
+        float l;
+        std::memcpy(&l, &lb, 4);
+        v += l;
+      }
+      outs[w][i] = v;
+    }
+  }
+  return TTT_OK;
+}
+
 extern "C" int ttt_reset(ttt_ctx* c) {
   if (!c) return TTT_ERR_ARG;
   if (!c->loaded) return fail(c, TTT_ERR_STATE, "weights not loaded");
