@@ -127,6 +127,22 @@ def cpu_sample(shape, blob, tokens, n_tok):
     return n_tok / dt, cores, dt
 
 
+def max_over_ranks(x, dist, device):
+    """The largest value of x over all ranks (the slowest replica's time); x when single-process."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_tokens_per_s(world, steps, tokens_per_step, seconds):
+    """Whole-job throughput of `world` independent replicas, each processing
+    tokens_per_step tokens per step, timed by the slowest one."""
+    return world * steps * tokens_per_step / seconds
+
+
 def workload_name(s):
     return (f"{s.n_layers}L d{s.d_model} H{s.n_heads} f{s.d_ff} V{s.vocab} k{s.window} b{s.chunk} "
             f"theta{s.rope_theta:g} eta{s.eta:g} {s.compute}: {s.n_seqs} x {s.seq_len} tokens")
@@ -226,11 +242,7 @@ def run_ours(a):
     if not np.all(np.isfinite(losses)):
         raise RuntimeError(f"non-finite chunk losses: {losses}")
 
-    ms_max = ms
-    if dist is not None:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
+    ms_max = max_over_ranks(ms, dist, "cuda")
 
     # ------------------------------------------------------------ end-to-end (host buffers)
     e2e_steps = max(1, min(a.steps, 2))
@@ -250,17 +262,13 @@ def run_ours(a):
             m._check(T.ttt_prefill_chunk(m._h, base_t + 4 * s0, n, base_n + 4 * ci, base_l + 4 * ci),
                      "ttt_prefill_chunk")
     torch.cuda.synchronize()
-    e2e_s = time.perf_counter() - t0
-    if dist is not None:
-        t = torch.tensor([e2e_s], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(time.perf_counter() - t0, dist, "cuda")
     barrier()
 
     # --------------------------------------------------------------- reporting (rank 0)
     pk = peaks()
     alg = algorithmic_flops(shape, Tn)
-    value = world * a.steps * Tn / (ms_max / 1e3)
+    value = replica_tokens_per_s(world, a.steps, Tn, ms_max / 1e3)
     tc_frac = alg * a.steps / (ms / 1e3) / (pk["tc_sus"] * 1e12)
     total_ms = sum(v["ms"] for v in prof.values())
     avg_launch_ms = dom["ms"] / dom["launches"]
@@ -298,7 +306,7 @@ def run_ours(a):
            "tc_roofline_frac": tc_frac,
            "tc_roofline_frac_of_burst": tc_frac * pk["tc_sus"] / pk["tc"],
            "roofline": roof, "kernels": kernels, "clocks": clk, "gpu_launches": launches,
-           "e2e": {"value": world * e2e_steps * Tn / e2e_s, "unit": UNIT, "h2d_bytes_per_step": 4 * Tn + 4 * nc,
+           "e2e": {"value": replica_tokens_per_s(world, e2e_steps, Tn, e2e_s), "unit": UNIT, "h2d_bytes_per_step": 4 * Tn + 4 * nc,
                    "d2h_bytes_per_step": 4 * nc, "api": "ttt_prefill_chunk per chunk, pinned host buffers"},
            "final_chunk_loss": float(losses[-1])}
     if world == 1 and not a.no_cpu_baseline:
