@@ -143,6 +143,25 @@ def replica_tokens_per_s(world, steps, tokens_per_step, seconds):
     return world * steps * tokens_per_step / seconds
 
 
+# DRAM bytes (read + write) of one steady-state launch (window full) of the attention
+# forward at the 760M shape, from `ncu --set full` captures (profiles/attn_fwd_760m.md):
+# the frozen-block pass over 4096 queries, and a trainable block over one 1024-token chunk.
+ATTN_FWD_TRAFFIC_760M = {"pass": 88.28e6 + 5.47e6, "step": 59.83e6 + 0.97e6}
+
+
+def attn_fwd_traffic(shape, nc):
+    """Average DRAM bytes per attention-forward launch over one step's launch mix (760M
+    shape only; earlier chunks see partial windows and move fewer bytes, so this is an
+    upper estimate), else None."""
+    if (shape.n_layers, shape.d_model, shape.window, shape.chunk) != (24, 1536, 8192, 1024):
+        return None
+    G = max(1, min(4096 // shape.chunk, shape.window // shape.chunk))
+    passes = -(-nc // G) * (shape.n_layers - shape.n_trainable)
+    steps = nc * shape.n_trainable
+    t = ATTN_FWD_TRAFFIC_760M
+    return (passes * t["pass"] + steps * t["step"]) / (passes + steps)
+
+
 def workload_name(s):
     return (f"{s.n_layers}L d{s.d_model} H{s.n_heads} f{s.d_ff} V{s.vocab} k{s.window} b{s.chunk} "
             f"theta{s.rope_theta:g} eta{s.eta:g} {s.compute}: {s.n_seqs} x {s.seq_len} tokens")
@@ -275,7 +294,8 @@ def run_ours(a):
     if dom["alg_flops"] > 0:
         ach = dom["alg_flops"] / (dom["ms"] / 1e3) / 1e12
         roof = {"kernel": dom_name, "bound": "tensor", "achieved": ach, "peak": pk["tc_sus"], "unit": "TFLOP/s",
-                "frac": ach / pk["tc_sus"], "traffic": None,
+                "frac": ach / pk["tc_sus"],
+                "traffic": attn_fwd_traffic(shape, nc) if dom_name == "attn_fwd" else None,
                 "peak_source": f"bf16_tflops_sustained ({pk['kind']}); burst {pk['tc']}",
                 "frac_of_burst": ach / pk["tc"], "avg_launch_ms": avg_launch_ms,
                 "launches_timed": dom["launches"], "alg_flops_per_launch": dom["alg_flops"] / dom["launches"]}
