@@ -183,6 +183,7 @@ TTT_DEV void load_f32_32(const float* p, float (&v)[32], int ncols) {
 }
 
 constexpr int kGemmThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue (two per TMEM lane quadrant)
+constexpr int kXposeBytes = 8 * 32 * 33 * 4;  // elementwise epilogues: a 32 x 33 fp32 buffer per epilogue warp
 
 template <int BN, bool SPLIT, int EPI, int DH>
 __global__ void __launch_bounds__(kGemmThreads, 1)
@@ -198,6 +199,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // elementwise epilogues: one 32 x 33 fp32 transpose buffer per epilogue warp, after the barriers
+  float* xpose = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE + 256);
+  constexpr bool kCoalesced = EPI == EPI_F32 || EPI == EPI_OPND || EPI == EPI_RESID || EPI == EPI_GELU ||
+                              EPI == EPI_GELU_BWD || EPI == EPI_SGD;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mt = (g.M + BM - 1) / BM, nt = (g.N + BN - 1) / BN, ntiles = mt * nt;
@@ -381,6 +386,112 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           store_opnd_n<DH>(oh, ol, (long)row * g.rd + scol + hh * DH, v);
         }
+      } else if constexpr (kCoalesced) {
+        // Elementwise epilogues with coalesced global traffic: the accumulator (one row
+        // per lane) goes through a 32 x 33 shared-memory transpose so that each lane then
+        // owns 4 consecutive columns of rows lr, lr+4, ..., lr+28 of the warp's 32 rows,
+        // and every load, store or reduction of the warp covers four whole 128-B row
+        // segments.  The epilogue's fp32 operand (residual, GELU argument, weights) is
+        // fetched one chunk ahead in the same layout.
+        float* xs = xpose + (warp - 2) * (32 * 33);
+        const int r0 = mtile * BM + q * 32;
+        const int lr = lane >> 3, lc = (lane & 7) * 4;
+        const bool sliced = (EPI == EPI_F32 || EPI == EPI_RESID) && ks > 1;
+        constexpr bool kIn = EPI == EPI_RESID || EPI == EPI_GELU_BWD || EPI == EPI_SGD;
+        const float* gin = EPI == EPI_RESID ? g.resid : (EPI == EPI_GELU_BWD ? g.aux : g.w32);
+        const long ldin = EPI == EPI_RESID ? g.ldr : (EPI == EPI_GELU_BWD ? g.ldaux : g.ldw);
+        float4 pn[8] = {};
+        auto load_in = [&](int c0) {
+          if constexpr (kIn) {
+            if (sliced) return;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int rr = r0 + lr + 4 * i;
+              pn[i] = (rr < g.M && c0 + lc + 3 < g.N)
+                          ? *reinterpret_cast<const float4*>(gin + (long)rr * ldin + c0 + lc)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+          }
+        };
+        // one element of the epilogue: acc -> (fp32 result, bf16-operand result)
+        auto elem = [&](float acc, float in, float& f32, float& opnd) {
+          if (EPI == EPI_F32) { f32 = acc; }
+          else if (EPI == EPI_OPND) { opnd = acc; }
+          else if (EPI == EPI_RESID) { f32 = in + acc; }
+          else if (EPI == EPI_GELU) { f32 = acc; opnd = gelu_f(acc, exact); }
+          else if (EPI == EPI_GELU_BWD) { opnd = acc * gelu_grad_f(in, exact); }
+          else if (EPI == EPI_SGD) { f32 = in - g.eta * acc; opnd = f32; }
+        };
+        float* out32 = EPI == EPI_SGD ? g.w32 : g.out32;
+        const long ld32 = EPI == EPI_SGD ? g.ldw : g.ldo32;
+        bf16* oh = EPI == EPI_SGD ? g.wh : g.oh;
+        bf16* ol = EPI == EPI_SGD ? g.wl : g.ol;
+        const long ldh = EPI == EPI_SGD ? g.ldw : g.ldo;
+        constexpr bool kF32Out = EPI == EPI_F32 || EPI == EPI_RESID || EPI == EPI_GELU || EPI == EPI_SGD;
+        constexpr bool kOpndOut = EPI == EPI_OPND || EPI == EPI_GELU || EPI == EPI_GELU_BWD || EPI == EPI_SGD;
+        load_in(n0 + half * 32);
+#pragma unroll 1
+        for (int c = half; c < BN / 32; c += 2) {
+          const int c0 = n0 + c * 32;
+          float v[32];
+          tmem_ld32(taddr + (uint32_t)(c * 32), v);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) xs[lane * 33 + j] = v[j];
+          __syncwarp();
+          float4 in4[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) in4[i] = pn[i];
+          if (c + 2 < BN / 32) load_in(c0 + 64);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int rl = lr + 4 * i, rr = r0 + rl;
+            if (rr >= g.M || c0 + lc >= g.N) continue;
+            const float* a4 = xs + rl * 33 + lc;
+            const long o32 = (long)rr * ld32 + c0 + lc, oh_off = (long)rr * ldh + c0 + lc;
+            if (c0 + lc + 3 < g.N) {
+              const float inv[4] = {in4[i].x, in4[i].y, in4[i].z, in4[i].w};
+              float f[4] = {0.f, 0.f, 0.f, 0.f}, o[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) elem(a4[e], inv[e], f[e], o[e]);
+              if (sliced) {
+                asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(g.out32 + o32), "f"(a4[0]),
+                             "f"(a4[1]), "f"(a4[2]), "f"(a4[3])
+                             : "memory");
+                continue;
+              }
+              if (kF32Out && out32) *reinterpret_cast<float4*>(out32 + o32) = make_float4(f[0], f[1], f[2], f[3]);
+              if (kOpndOut) {
+                __nv_bfloat162 t0 = __floats2bfloat162_rn(o[0], o[1]), t1 = __floats2bfloat162_rn(o[2], o[3]);
+                uint2 hv;
+                hv.x = *reinterpret_cast<uint32_t*>(&t0);
+                hv.y = *reinterpret_cast<uint32_t*>(&t1);
+                *reinterpret_cast<uint2*>(oh + oh_off) = hv;
+                if (ol) {
+                  const float2 f0 = __bfloat1622float2(t0), f1 = __bfloat1622float2(t1);
+                  uint2 lv;
+                  lv.x = pack_bf16(o[0] - f0.x, o[1] - f0.y);
+                  lv.y = pack_bf16(o[2] - f1.x, o[3] - f1.y);
+                  *reinterpret_cast<uint2*>(ol + oh_off) = lv;
+                }
+              }
+            } else {  // ragged right edge: scalar, the operand read directly
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                if (c0 + lc + e >= g.N) continue;
+                if (sliced) {
+                  atomicAdd(g.out32 + o32 + e, a4[e]);
+                  continue;
+                }
+                const float in = kIn ? gin[(long)rr * ldin + c0 + lc + e] : 0.f;
+                float f = 0.f, o = 0.f;
+                elem(a4[e], in, f, o);
+                if (kF32Out && out32) out32[o32 + e] = f;
+                if (kOpndOut) store_opnd(oh, ol, oh_off + e, o);
+              }
+            }
+          }
+          __syncwarp();
+        }
       } else {
       // Global operand of the epilogue (residual, GELU argument, fp32 weights), fetched
       // one chunk ahead so that its latency overlaps the current chunk's work.
@@ -485,15 +596,19 @@ int launch(const CUtensorMap& a, const CUtensorMap& al, const CUtensorMap& b, co
            const GemmArgs& g, cudaStream_t st) {
   using C = Cfg<BN, SPLIT>;
   auto kern = gemm_kernel<BN, SPLIT, EPI, DH>;
+  constexpr bool kCo = EPI == EPI_F32 || EPI == EPI_OPND || EPI == EPI_RESID || EPI == EPI_GELU ||
+                      EPI == EPI_GELU_BWD || EPI == EPI_SGD;
+  constexpr int SMEM = C::SMEM + (kCo ? kXposeBytes : 0);
+  static_assert(SMEM <= 232448, "GEMM exceeds shared memory");
   static bool attr_set = false;  // per instantiation
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return (int)e;
     attr_set = true;
   }
   const int tiles = ((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN) * (g.ksplit > 1 ? g.ksplit : 1);
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  return (int)launch_k(kern, dim3(grid), dim3(kGemmThreads), C::SMEM, st, a, al, b, bl, g);
+  return (int)launch_k(kern, dim3(grid), dim3(kGemmThreads), SMEM, st, a, al, b, bl, g);
 }
 
 template <int BN, bool SPLIT>
