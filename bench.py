@@ -146,13 +146,16 @@ def replica_tokens_per_s(world, steps, tokens_per_step, seconds):
 # DRAM bytes (read + write) of one steady-state launch (window full) of the attention
 # forward at the 760M shape, from `ncu --set full` captures (profiles/attn_fwd_760m.md):
 # the frozen-block pass over 4096 queries, and a trainable block over one 1024-token chunk.
-ATTN_FWD_TRAFFIC_760M = {"pass": 88.28e6 + 5.47e6, "step": 59.83e6 + 0.97e6}
+# None until the current forward kernel has been captured.
+ATTN_FWD_TRAFFIC_760M = None
 
 
 def attn_fwd_traffic(shape, nc):
     """Average DRAM bytes per attention-forward launch over one step's launch mix (760M
     shape only; earlier chunks see partial windows and move fewer bytes, so this is an
     upper estimate), else None."""
+    if ATTN_FWD_TRAFFIC_760M is None:
+        return None
     if (shape.n_layers, shape.d_model, shape.window, shape.chunk) != (24, 1536, 8192, 1024):
         return None
     G = max(1, min(4096 // shape.chunk, shape.window // shape.chunk))

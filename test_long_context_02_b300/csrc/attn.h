@@ -25,10 +25,11 @@ struct AttnMaps {
 };
 
 int attn_fwd_run(const AttnMaps& m, const AttnArgs& a, bool split, cudaStream_t st);
-// bf16 operands only: two query tiles per CTA, P kept in TMEM (attn_fwd2.cu).
-int attn_fwd2_run(const AttnMaps& m, const AttnArgs& a, cudaStream_t st);
 // One query tile per CTA, P and O kept in TMEM (attn_fwd3.cu).
 int attn_fwd3_run(const AttnMaps& m, const AttnArgs& a, bool split, cudaStream_t st);
+// bf16 operands only: one query tile per CTA, two softmax warpgroups on alternate key
+// tiles, each with its own O accumulator in TMEM (attn_fwd5.cu).
+int attn_fwd5_run(const AttnMaps& m, const AttnArgs& a, cudaStream_t st);
 
 // Backward: geometry from g; lse ([H][n], log2 domain) from the forward;
 // D[h][t] = rowsum(dO * O); outputs dq (all keys) and dk, dv (own keys only),

@@ -6,10 +6,11 @@
 // cache holds only the window; §8 FAQ Q4, any k >= b), keys before the chunk
 // from the k-slot cache and the chunk's own keys from its own K/V buffer, and
 // write O (bf16 hi [+ lo]) and the per-row log2-sum-exp for the backward.
-//   attn_fwd3.cu: one 128-query tile per CTA, P and O in tensor memory (both
-//                 compute modes);
-//   attn_fwd2.cu: two 128-query tiles per CTA sharing every K/V tile (bf16
-//                 operands), used when its grid makes at least two full waves.
+//   attn_fwd5.cu: bf16 operands; one 128-query tile per CTA, two softmax
+//                 warpgroups on alternate key tiles, each with its own O
+//                 accumulator in tensor memory;
+//   attn_fwd3.cu: split (fp32) mode; one 128-query tile per CTA, two threads
+//                 per query row, P and O in tensor memory.
 #include "attn.h"
 #include "kernels.h"
 
@@ -17,7 +18,7 @@ namespace ttt {
 
 int attn_fwd_run(const AttnMaps& m, const AttnArgs& a, bool split, cudaStream_t st) {
   if (a.n <= 0) return 0;
-  if (!split && (long)((a.n + 255) / 256) * a.H >= 2L * num_sms()) return attn_fwd2_run(m, a, st);
+  if (!split) return attn_fwd5_run(m, a, st);
   return attn_fwd3_run(m, a, split, st);
 }
 
