@@ -195,56 +195,57 @@ __global__ void __launch_bounds__(kK2Threads, 1)
       for (int s = 0; s < 2; ++s)
         if (iss & (1u << s)) drain_k2(&qd_full[s], (ipar >> s) & 1u, g.err);
     }
-  } else if (warp == 1) {
-    if (lane == 0) {  // ------------------------------------------------------ MMA issuer
-      constexpr uint32_t idSS = idesc_bf16(128, 128, 0, 0);
-      constexpr uint32_t idAcc = idesc_bf16(128, DH, 0, 1);
-      const uint32_t kb = smem_u32(smem + C::K_OFF), vb = smem_u32(smem + C::V_OFF);
-      auto xy = [&](uint32_t d, uint32_t xb, uint32_t yb) {  // d = X Y^T over the head dim
+  } else if (warp == 1) {  // MMA issuer: the whole warp, one elected lane issues
+    auto wait_all = [&](uint64_t* bar, uint32_t par) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait(bar, par, abort_flag, g.err, DERR_TIMEOUT_MMA));
+    };
+    constexpr uint32_t idSS = idesc_bf16(128, 128, 0, 0);
+    constexpr uint32_t idAcc = idesc_bf16(128, DH, 0, 1);
+    const uint32_t kb = smem_u32(smem + C::K_OFF), vb = smem_u32(smem + C::V_OFF);
+    auto xy = [&](uint32_t d, uint32_t xb, uint32_t yb) {  // d = X Y^T over the head dim
 #pragma unroll
-        for (int kk = 0; kk < DH / 16; ++kk) {
-          mma_bf16(d, kdesc_k2(xb, kk), kdesc_k2(yb, kk), idSS, kk ? 1u : 0u);
-          if (SPLIT) {
-            mma_bf16(d, kdesc_k2(xb, kk), kdesc_k2(yb + C::TILE, kk), idSS, 1u);
-            mma_bf16(d, kdesc_k2(xb + C::TILE, kk), kdesc_k2(yb, kk), idSS, 1u);
-          }
+      for (int kk = 0; kk < DH / 16; ++kk) {
+        mma_bf16_w(d, kdesc_k2(xb, kk), kdesc_k2(yb, kk), idSS, kk ? 1u : 0u);
+        if (SPLIT) {
+          mma_bf16_w(d, kdesc_k2(xb, kk), kdesc_k2(yb + C::TILE, kk), idSS, 1u);
+          mma_bf16_w(d, kdesc_k2(xb + C::TILE, kk), kdesc_k2(yb, kk), idSS, 1u);
         }
-      };
-      // d (+)= A Y with A (128 keys x 128 queries, bf16) in TMEM: query columns 0-63 at
-      // [a0, a0+32) (+ remainders [a0+32, a0+64)), 64-127 at [a0+64, a0+96) (+ [a0+96, a0+128))
-      auto acc = [&](uint32_t d, uint32_t a0, uint32_t yb, bool first) {
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t pa = a0 + (uint32_t)((kk < 4 ? 0 : 64) + 8 * (kk & 3));
-          mma_bf16_ts(d, pa, mndesc_k2(yb, kk), idAcc, (!first || kk) ? 1u : 0u);
-          if (SPLIT) {
-            mma_bf16_ts(d, pa, mndesc_k2(yb + C::TILE, kk), idAcc, 1u);
-            mma_bf16_ts(d, pa + 32u, mndesc_k2(yb, kk), idAcc, 1u);
-          }
-        }
-      };
-      bool ok = I > 0 && mbar_wait(kv_full, 0, abort_flag, g.err, DERR_TIMEOUT_MMA);
-      for (int i = 0; i < I && ok; ++i) {
-        const int s = i & 1;
-        if (!mbar_wait(&qd_full[s], (uint32_t)((i >> 1) & 1), abort_flag, g.err, DERR_TIMEOUT_MMA)) break;
-        tc_fence_after();
-        const uint32_t qb = smem_u32(smem + C::Q_OFF + s * C::STAGE);
-        const uint32_t dob = qb + C::NOP * C::TILE;
-        xy(tmem + T_S, kb, qb);    // S^T = K Q^T   (P^T, dS^T of tile i-1 were consumed above)
-        xy(tmem + T_DP, vb, dob);  // dP^T = V dO^T
-        mma_commit(s_full);
-        if (!mbar_wait(p_full, (uint32_t)(i & 1), abort_flag, g.err, DERR_TIMEOUT_MMA)) break;
-        tc_fence_after();
-        acc(tmem + T_DV, tmem + T_S, dob, i == 0);  // dV += P^T dO
-        if (!mbar_wait(ds_full, (uint32_t)(i & 1), abort_flag, g.err, DERR_TIMEOUT_MMA)) break;
-        tc_fence_after();
-        acc(tmem + T_DK, tmem + T_DP, qb, i == 0);  // dK += dS^T Q
-        mma_commit(&qd_empty[s]);
       }
-      mma_commit(acc_full);
-      mma_commit(drain);
-      drain_k2(drain, 0, g.err);
+    };
+    // d (+)= A Y with A (128 keys x 128 queries, bf16) in TMEM: query columns 0-63 at
+    // [a0, a0+32) (+ remainders [a0+32, a0+64)), 64-127 at [a0+64, a0+96) (+ [a0+96, a0+128))
+    auto acc = [&](uint32_t d, uint32_t a0, uint32_t yb, bool first) {
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t pa = a0 + (uint32_t)((kk < 4 ? 0 : 64) + 8 * (kk & 3));
+        mma_bf16_ts_w(d, pa, mndesc_k2(yb, kk), idAcc, (!first || kk) ? 1u : 0u);
+        if (SPLIT) {
+          mma_bf16_ts_w(d, pa, mndesc_k2(yb + C::TILE, kk), idAcc, 1u);
+          mma_bf16_ts_w(d, pa + 32u, mndesc_k2(yb, kk), idAcc, 1u);
+        }
+      }
+    };
+    bool ok = I > 0 && wait_all(kv_full, 0);
+    for (int i = 0; i < I && ok; ++i) {
+      const int s = i & 1;
+      if (!wait_all(&qd_full[s], (uint32_t)((i >> 1) & 1))) break;
+      tc_fence_after();
+      const uint32_t qb = smem_u32(smem + C::Q_OFF + s * C::STAGE);
+      const uint32_t dob = qb + C::NOP * C::TILE;
+      xy(tmem + T_S, kb, qb);    // S^T = K Q^T   (P^T, dS^T of tile i-1 were consumed above)
+      xy(tmem + T_DP, vb, dob);  // dP^T = V dO^T
+      mma_commit_w(s_full);
+      if (!wait_all(p_full, (uint32_t)(i & 1))) break;
+      tc_fence_after();
+      acc(tmem + T_DV, tmem + T_S, dob, i == 0);  // dV += P^T dO
+      if (!wait_all(ds_full, (uint32_t)(i & 1))) break;
+      tc_fence_after();
+      acc(tmem + T_DK, tmem + T_DP, qb, i == 0);  // dK += dS^T Q
+      mma_commit_w(&qd_empty[s]);
     }
+    mma_commit_w(acc_full);
+    mma_commit_w(drain);
+    drain_k2(drain, 0, g.err);
   } else {  // ------------------------------------------- softmax: two threads per key row (64 queries)
     const int hf = (warp - 2) >> 2, qd = warp & 3, r = qd * 32 + lane;
     const int krow = 128 * kt + r;

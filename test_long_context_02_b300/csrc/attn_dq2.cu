@@ -198,61 +198,62 @@ __global__ void __launch_bounds__(kQ2Threads, 1)
         if (viss & (1u << s)) drain_q2(&v_full[s], (vpar >> s) & 1u, g.err);
       }
     }
-  } else if (warp == 1) {
-    if (lane == 0) {  // ------------------------------------------------------ MMA issuer
-      constexpr uint32_t idSS = idesc_bf16(128, 128, 0, 0);
-      constexpr uint32_t idDQ = idesc_bf16(128, DH, 0, 1);
-      const uint32_t qb = smem_u32(smem + C::Q_OFF), dob = smem_u32(smem + C::DO_OFF);
-      auto xk = [&](uint32_t d, uint32_t xb, uint32_t kb) {  // d = X K^T over the head dim
+  } else if (warp == 1) {  // MMA issuer: the whole warp, one elected lane issues
+    auto wait_all = [&](uint64_t* bar, uint32_t par) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait(bar, par, abort_flag, g.err, DERR_TIMEOUT_MMA));
+    };
+    constexpr uint32_t idSS = idesc_bf16(128, 128, 0, 0);
+    constexpr uint32_t idDQ = idesc_bf16(128, DH, 0, 1);
+    const uint32_t qb = smem_u32(smem + C::Q_OFF), dob = smem_u32(smem + C::DO_OFF);
+    auto xk = [&](uint32_t d, uint32_t xb, uint32_t kb) {  // d = X K^T over the head dim
 #pragma unroll
-        for (int kk = 0; kk < DH / 16; ++kk) {
-          mma_bf16(d, kdesc_q2(xb, kk), kdesc_q2(kb, kk), idSS, kk ? 1u : 0u);
-          if (SPLIT) {
-            mma_bf16(d, kdesc_q2(xb, kk), kdesc_q2(kb + C::TILE, kk), idSS, 1u);
-            mma_bf16(d, kdesc_q2(xb + C::TILE, kk), kdesc_q2(kb, kk), idSS, 1u);
-          }
+      for (int kk = 0; kk < DH / 16; ++kk) {
+        mma_bf16_w(d, kdesc_q2(xb, kk), kdesc_q2(kb, kk), idSS, kk ? 1u : 0u);
+        if (SPLIT) {
+          mma_bf16_w(d, kdesc_q2(xb, kk), kdesc_q2(kb + C::TILE, kk), idSS, 1u);
+          mma_bf16_w(d, kdesc_q2(xb + C::TILE, kk), kdesc_q2(kb, kk), idSS, 1u);
         }
-      };
-      bool ok = J > 0 && mbar_wait(q_full, 0, abort_flag, g.err, DERR_TIMEOUT_MMA) &&
-                mbar_wait(&k_full[0], 0, abort_flag, g.err, DERR_TIMEOUT_MMA);
-      if (ok) {
-        tc_fence_after();
-        xk(tmem, qb, smem_u32(smem + C::K_OFF));  // S_0
       }
-      for (int j = 0; j < J && ok; ++j) {
-        const int s = j & 1;
-        if (!mbar_wait(&v_full[s], (uint32_t)((j >> 1) & 1), abort_flag, g.err, DERR_TIMEOUT_MMA)) break;
-        tc_fence_after();
-        // dP_j = dO V_j^T (the softmax finished reading dP_{j-1} before dS_{j-1} was signalled)
-        xk(tmem + T_DP, dob, smem_u32(smem + C::V_OFF + s * C::NOP * C::TILE));
-        mma_commit(&s_full[s]);
-        mma_commit(&v_empty[s]);
-        if (j + 1 < J) {  // S_{j+1} into the other buffer: its dS_{j-1} K_{j-1} product was issued last round
-          if (!mbar_wait(&k_full[s ^ 1], (uint32_t)(((j + 1) >> 1) & 1), abort_flag, g.err, DERR_TIMEOUT_MMA)) break;
-          tc_fence_after();
-          xk(tmem + (uint32_t)((s ^ 1) * 128), qb, smem_u32(smem + C::K_OFF + (s ^ 1) * C::NOP * C::TILE));
-        }
-        if (!mbar_wait(&ds_full[s], (uint32_t)((j >> 1) & 1), abort_flag, g.err, DERR_TIMEOUT_MMA)) break;
-        tc_fence_after();
-        // dQ += dS_j K_j; dS_j: keys 0-63 in columns [0,32) (+ remainders [32,64)), keys 64-127 in
-        // [64,96) (+ [96,128)) of score buffer s
-        const uint32_t kb = smem_u32(smem + C::K_OFF + s * C::NOP * C::TILE);
-        const uint32_t pb = tmem + (uint32_t)(s * 128);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t pa = pb + (uint32_t)((kk < 4 ? 0 : 64) + 8 * (kk & 3));
-          mma_bf16_ts(tmem + T_DQ, pa, mndesc_q2(kb, kk), idDQ, (j | kk) ? 1u : 0u);
-          if (SPLIT) {
-            mma_bf16_ts(tmem + T_DQ, pa, mndesc_q2(kb + C::TILE, kk), idDQ, 1u);
-            mma_bf16_ts(tmem + T_DQ, pa + 32u, mndesc_q2(kb, kk), idDQ, 1u);
-          }
-        }
-        mma_commit(&k_empty[s]);
-      }
-      mma_commit(dq_full);
-      mma_commit(drain);
-      drain_q2(drain, 0, g.err);
+    };
+    bool ok = J > 0 && wait_all(q_full, 0) &&
+              wait_all(&k_full[0], 0);
+    if (ok) {
+      tc_fence_after();
+      xk(tmem, qb, smem_u32(smem + C::K_OFF));  // S_0
     }
+    for (int j = 0; j < J && ok; ++j) {
+      const int s = j & 1;
+      if (!wait_all(&v_full[s], (uint32_t)((j >> 1) & 1))) break;
+      tc_fence_after();
+      // dP_j = dO V_j^T (the softmax finished reading dP_{j-1} before dS_{j-1} was signalled)
+      xk(tmem + T_DP, dob, smem_u32(smem + C::V_OFF + s * C::NOP * C::TILE));
+      mma_commit_w(&s_full[s]);
+      mma_commit_w(&v_empty[s]);
+      if (j + 1 < J) {  // S_{j+1} into the other buffer: its dS_{j-1} K_{j-1} product was issued last round
+        if (!wait_all(&k_full[s ^ 1], (uint32_t)(((j + 1) >> 1) & 1))) break;
+        tc_fence_after();
+        xk(tmem + (uint32_t)((s ^ 1) * 128), qb, smem_u32(smem + C::K_OFF + (s ^ 1) * C::NOP * C::TILE));
+      }
+      if (!wait_all(&ds_full[s], (uint32_t)((j >> 1) & 1))) break;
+      tc_fence_after();
+      // dQ += dS_j K_j; dS_j: keys 0-63 in columns [0,32) (+ remainders [32,64)), keys 64-127 in
+      // [64,96) (+ [96,128)) of score buffer s
+      const uint32_t kb = smem_u32(smem + C::K_OFF + s * C::NOP * C::TILE);
+      const uint32_t pb = tmem + (uint32_t)(s * 128);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t pa = pb + (uint32_t)((kk < 4 ? 0 : 64) + 8 * (kk & 3));
+        mma_bf16_ts_w(tmem + T_DQ, pa, mndesc_q2(kb, kk), idDQ, (j | kk) ? 1u : 0u);
+        if (SPLIT) {
+          mma_bf16_ts_w(tmem + T_DQ, pa, mndesc_q2(kb + C::TILE, kk), idDQ, 1u);
+          mma_bf16_ts_w(tmem + T_DQ, pa + 32u, mndesc_q2(kb, kk), idDQ, 1u);
+        }
+      }
+      mma_commit_w(&k_empty[s]);
+    }
+    mma_commit_w(dq_full);
+    mma_commit_w(drain);
+    drain_q2(drain, 0, g.err);
   } else {  // ------------------------------------------------- softmax: two threads per query row
     const int hf = (warp - 2) >> 2, qd = warp & 3, r = qd * 32 + lane;
     const long p = g.pos0 + 128L * qt + r;

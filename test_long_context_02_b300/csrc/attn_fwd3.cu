@@ -218,63 +218,64 @@ __global__ void __launch_bounds__(kF3Threads, 1)
         if (viss & (1u << s)) drain3(&v_full[s], (vpar >> s) & 1u, a.err);
       }
     }
-  } else if (warp == 1) {
-    if (lane == 0) {  // -------------------------------------------------------- MMA issuer
-      constexpr uint32_t idS = idesc_bf16(128, 128, 0, 0);
-      constexpr uint32_t idPV = idesc_bf16(128, DH, 0, 1);
-      const uint32_t q0 = smem_u32(smem + C::Q_OFF);
-      auto issue_s = [&](int j) {  // S_j = Q K_j^T into score buffer j & 1
-        const int s = j & 1;
-        const uint32_t kb = smem_u32(smem + C::K_OFF + s * C::NOP * C::TILE);
-        const uint32_t d = tmem + (uint32_t)(s * 128);
+  } else if (warp == 1) {  // MMA issuer: the whole warp, one elected lane issues
+    auto wait_all = [&](uint64_t* bar, uint32_t par) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait(bar, par, abort_flag, a.err, DERR_TIMEOUT_MMA));
+    };
+    constexpr uint32_t idS = idesc_bf16(128, 128, 0, 0);
+    constexpr uint32_t idPV = idesc_bf16(128, DH, 0, 1);
+    const uint32_t q0 = smem_u32(smem + C::Q_OFF);
+    auto issue_s = [&](int j) {  // S_j = Q K_j^T into score buffer j & 1
+      const int s = j & 1;
+      const uint32_t kb = smem_u32(smem + C::K_OFF + s * C::NOP * C::TILE);
+      const uint32_t d = tmem + (uint32_t)(s * 128);
 #pragma unroll
-        for (int kk = 0; kk < DH / 16; ++kk) {
-          mma_bf16(d, kdesc3(q0, kk), kdesc3(kb, kk), idS, kk ? 1u : 0u);
-          if (SPLIT) {
-            mma_bf16(d, kdesc3(q0, kk), kdesc3(kb + C::TILE, kk), idS, 1u);
-            mma_bf16(d, kdesc3(q0 + C::TILE, kk), kdesc3(kb, kk), idS, 1u);
-          }
+      for (int kk = 0; kk < DH / 16; ++kk) {
+        mma_bf16_w(d, kdesc3(q0, kk), kdesc3(kb, kk), idS, kk ? 1u : 0u);
+        if (SPLIT) {
+          mma_bf16_w(d, kdesc3(q0, kk), kdesc3(kb + C::TILE, kk), idS, 1u);
+          mma_bf16_w(d, kdesc3(q0 + C::TILE, kk), kdesc3(kb, kk), idS, 1u);
         }
-        mma_commit(&s_full[s]);
-        mma_commit(&k_empty[s]);
-      };
-      bool ok = J > 0 && mbar_wait(q_full, 0, abort_flag, a.err, DERR_TIMEOUT_MMA) &&
-                mbar_wait(&k_full[0], 0, abort_flag, a.err, DERR_TIMEOUT_MMA);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0);
       }
-      for (int j = 0; j < J && ok; ++j) {
-        const int s = j & 1;
-        if (j + 1 < J) {  // next scores into the other buffer, whose P V product was issued last round
-          if (!mbar_wait(&k_full[s ^ 1], (uint32_t)(((j + 1) >> 1) & 1), abort_flag, a.err, DERR_TIMEOUT_MMA)) break;
-          tc_fence_after();
-          issue_s(j + 1);
-        }
-        if (!mbar_wait(&p_full[s], (uint32_t)((j >> 1) & 1), abort_flag, a.err, DERR_TIMEOUT_MMA)) break;
-        if (!mbar_wait(&v_full[s], (uint32_t)((j >> 1) & 1), abort_flag, a.err, DERR_TIMEOUT_MMA)) break;
-        tc_fence_after();
-        // O += P_j V_j; P_j: keys 0-63 in columns [0,32) (+ remainders [32,64)), keys 64-127 in
-        // columns [64,96) (+ [96,128)) of score buffer s
-        const uint32_t pb = tmem + (uint32_t)(s * 128);
-        const uint32_t vb = smem_u32(smem + C::V_OFF + s * C::NOP * C::TILE);
-        const uint32_t d = tmem + 256u;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t pa = pb + (uint32_t)((kk < 4 ? 0 : 64) + 8 * (kk & 3));
-          mma_bf16_ts(d, pa, mndesc3(vb, kk), idPV, (j | kk) ? 1u : 0u);
-          if (SPLIT) {
-            mma_bf16_ts(d, pa, mndesc3(vb + C::TILE, kk), idPV, 1u);
-            mma_bf16_ts(d, pa + 32u, mndesc3(vb, kk), idPV, 1u);
-          }
-        }
-        mma_commit(o_done);
-        mma_commit(&v_empty[s]);
-        if (j == J - 1) mma_commit(o_final);
-      }
-      mma_commit(drain);  // every MMA issued above has finished once this arrives
-      drain3(drain, 0, a.err);
+      mma_commit_w(&s_full[s]);
+      mma_commit_w(&k_empty[s]);
+    };
+    bool ok = J > 0 && wait_all(q_full, 0) &&
+              wait_all(&k_full[0], 0);
+    if (ok) {
+      tc_fence_after();
+      issue_s(0);
     }
+    for (int j = 0; j < J && ok; ++j) {
+      const int s = j & 1;
+      if (j + 1 < J) {  // next scores into the other buffer, whose P V product was issued last round
+        if (!wait_all(&k_full[s ^ 1], (uint32_t)(((j + 1) >> 1) & 1))) break;
+        tc_fence_after();
+        issue_s(j + 1);
+      }
+      if (!wait_all(&p_full[s], (uint32_t)((j >> 1) & 1))) break;
+      if (!wait_all(&v_full[s], (uint32_t)((j >> 1) & 1))) break;
+      tc_fence_after();
+      // O += P_j V_j; P_j: keys 0-63 in columns [0,32) (+ remainders [32,64)), keys 64-127 in
+      // columns [64,96) (+ [96,128)) of score buffer s
+      const uint32_t pb = tmem + (uint32_t)(s * 128);
+      const uint32_t vb = smem_u32(smem + C::V_OFF + s * C::NOP * C::TILE);
+      const uint32_t d = tmem + 256u;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t pa = pb + (uint32_t)((kk < 4 ? 0 : 64) + 8 * (kk & 3));
+        mma_bf16_ts_w(d, pa, mndesc3(vb, kk), idPV, (j | kk) ? 1u : 0u);
+        if (SPLIT) {
+          mma_bf16_ts_w(d, pa, mndesc3(vb + C::TILE, kk), idPV, 1u);
+          mma_bf16_ts_w(d, pa + 32u, mndesc3(vb, kk), idPV, 1u);
+        }
+      }
+      mma_commit_w(o_done);
+      mma_commit_w(&v_empty[s]);
+      if (j == J - 1) mma_commit_w(o_final);
+    }
+    mma_commit_w(drain);  // every MMA issued above has finished once this arrives
+    drain3(drain, 0, a.err);
   } else {  // --------------------------------------------------- softmax: two threads per query row
     const int hf = (warp - 2) >> 2;  // which 64 key columns (and which half of the head dim)
     const int qd = warp & 3;         // TMEM lane quadrant of this warp

@@ -187,50 +187,51 @@ __global__ void __launch_bounds__(kF5Threads, 1)
         if (viss & (1u << s)) drain5(&v_full[s], (vpar >> s) & 1u, a.err);
       }
     }
-  } else if (warp == 1) {
-    if (lane == 0) {  // -------------------------------------------------------- MMA issuer
-      constexpr uint32_t idS = idesc_bf16(128, 128, 0, 0);
-      constexpr uint32_t idPV = idesc_bf16(128, DH, 0, 1);
-      const uint32_t q0 = smem_u32(smem + C::Q_OFF);
-      auto issue_s = [&](int j) {  // S_j = Q K_j^T into buffer j & 1 (key stage j & 1)
-        const int s = j & 1;
-        const uint32_t kb = smem_u32(smem + C::K_OFF + s * C::TILE);
-        const uint32_t d = tmem + (uint32_t)(s * 128);
+  } else if (warp == 1) {  // ----------------------------- MMA issuer: the whole warp, one elected lane issues
+    constexpr uint32_t idS = idesc_bf16(128, 128, 0, 0);
+    constexpr uint32_t idPV = idesc_bf16(128, DH, 0, 1);
+    const uint32_t q0 = smem_u32(smem + C::Q_OFF);
+    auto wait_all = [&](uint64_t* bar, uint32_t par) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait(bar, par, abort_flag, a.err, DERR_TIMEOUT_MMA));
+    };
+    auto issue_s = [&](int j) {  // S_j = Q K_j^T into buffer j & 1 (key stage j & 1)
+      const int s = j & 1;
+      const uint32_t kb = smem_u32(smem + C::K_OFF + s * C::TILE);
+      const uint32_t d = tmem + (uint32_t)(s * 128);
 #pragma unroll
-        for (int kk = 0; kk < DH / 16; ++kk) mma_bf16(d, kdesc5(q0, kk), kdesc5(kb, kk), idS, kk ? 1u : 0u);
-        mma_commit(&s_full[s]);
-        mma_commit(&k_empty[s]);
-      };
-      bool ok = J > 0 && mbar_wait(q_full, 0, abort_flag, a.err, DERR_TIMEOUT_MMA);
-      for (int j = 0; j < 2 && j < J && ok; ++j) {
-        ok = mbar_wait(&k_full[j], 0, abort_flag, a.err, DERR_TIMEOUT_MMA);
-        if (ok) {
-          tc_fence_after();
-          issue_s(j);
-        }
-      }
-      for (int j = 0; j < J && ok; ++j) {
-        const int w = j & 1;
-        const uint32_t par = (uint32_t)((j >> 1) & 1);
-        if (!mbar_wait(&p_full[w], par, abort_flag, a.err, DERR_TIMEOUT_MMA)) break;
-        if (!mbar_wait(&v_full[w], par, abort_flag, a.err, DERR_TIMEOUT_MMA)) break;
+      for (int kk = 0; kk < DH / 16; ++kk) mma_bf16_w(d, kdesc5(q0, kk), kdesc5(kb, kk), idS, kk ? 1u : 0u);
+      mma_commit_w(&s_full[s]);
+      mma_commit_w(&k_empty[s]);
+    };
+    bool ok = J > 0 && wait_all(q_full, 0);
+    for (int j = 0; j < 2 && j < J && ok; ++j) {
+      ok = wait_all(&k_full[j], 0);
+      if (ok) {
         tc_fence_after();
-        const uint32_t pb = tmem + (uint32_t)(w * 128);  // P_j as bf16 pairs over the first 64 columns of S_w
-        const uint32_t vb = smem_u32(smem + C::V_OFF + w * C::TILE);
-        const uint32_t d = tmem + 256u + (uint32_t)(w * 128);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) mma_bf16_ts(d, pb + (uint32_t)(kk * 8), mndesc5(vb, kk), idPV, (j >= 2 || kk) ? 1u : 0u);
-        mma_commit(&v_empty[w]);
-        if (j + 2 >= J) mma_commit(&o_final[w]);
-        if (j + 2 < J) {  // after P_j V_j in issue order: S_{j+2} reuses buffer w
-          if (!mbar_wait(&k_full[w], (uint32_t)(((j + 2) >> 1) & 1), abort_flag, a.err, DERR_TIMEOUT_MMA)) break;
-          tc_fence_after();
-          issue_s(j + 2);
-        }
+        issue_s(j);
       }
-      mma_commit(drain);
-      drain5(drain, 0, a.err);
     }
+    for (int j = 0; j < J && ok; ++j) {
+      const int w = j & 1;
+      const uint32_t par = (uint32_t)((j >> 1) & 1);
+      if (!wait_all(&p_full[w], par)) break;
+      if (!wait_all(&v_full[w], par)) break;
+      tc_fence_after();
+      const uint32_t pb = tmem + (uint32_t)(w * 128);  // P_j as bf16 pairs over the first 64 columns of S_w
+      const uint32_t vb = smem_u32(smem + C::V_OFF + w * C::TILE);
+      const uint32_t d = tmem + 256u + (uint32_t)(w * 128);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) mma_bf16_ts_w(d, pb + (uint32_t)(kk * 8), mndesc5(vb, kk), idPV, (j >= 2 || kk) ? 1u : 0u);
+      mma_commit_w(&v_empty[w]);
+      if (j + 2 >= J) mma_commit_w(&o_final[w]);
+      if (j + 2 < J) {  // after P_j V_j in issue order: S_{j+2} reuses buffer w
+        if (!wait_all(&k_full[w], (uint32_t)(((j + 2) >> 1) & 1))) break;
+        tc_fence_after();
+        issue_s(j + 2);
+      }
+    }
+    mma_commit_w(drain);
+    drain5(drain, 0, a.err);
   } else {  // ---------------------------------- softmax: warpgroup w takes key tiles w, w+2, ...
     const int w = (warp - 2) >> 2;
     const int qd = warp & 3;

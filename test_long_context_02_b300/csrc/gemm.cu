@@ -278,52 +278,53 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int i = 0; i < C::STAGES; ++i)
         if (issued & (1u << i)) wait_drain(&full[i], (iss_par >> i) & 1u, g.err);
     }
-  } else if (warp == 1) {
-    if (lane == 0) {  // ------------------------------------------------ MMA issuer
-      const uint32_t idesc = idesc_bf16(BM, BN, g.a_mn, g.b_mn);
-      int s = 0;
-      uint32_t ph = 0;
-      int it = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++it) {
-        const int sl = u / ntiles;
-        const int kb0 = (int)((long)sl * nk / ks), kb1 = (int)((long)(sl + 1) * nk / ks);
-        const int buf = it & 1;
-        const uint32_t use = (uint32_t)(it >> 1);
-        if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag, g.err, DERR_TIMEOUT_MMA)) break;
+  } else if (warp == 1) {  // --------------------- MMA issuer: the whole warp, one elected lane issues
+    const uint32_t idesc = idesc_bf16(BM, BN, g.a_mn, g.b_mn);
+    auto wait_all = [&](uint64_t* bar, uint32_t par) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait(bar, par, abort_flag, g.err, DERR_TIMEOUT_MMA));
+    };
+    int s = 0;
+    uint32_t ph = 0;
+    int it = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++it) {
+      const int sl = u / ntiles;
+      const int kb0 = (int)((long)sl * nk / ks), kb1 = (int)((long)(sl + 1) * nk / ks);
+      const int buf = it & 1;
+      const uint32_t use = (uint32_t)(it >> 1);
+      if (!wait_all(&tempty[buf], (use & 1u) ^ 1u)) break;
+      tc_fence_after();
+      const uint32_t dt = tmem + (uint32_t)(buf * BN);
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!wait_all(&full[s], ph)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
-        const uint32_t dt = tmem + (uint32_t)(buf * BN);
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(&full[s], ph, abort_flag, g.err, DERR_TIMEOUT_MMA)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a = smem_u32(smem + s * C::STAGE);
-          const uint32_t b = a + C::A_BYTES;
+        const uint32_t a = smem_u32(smem + s * C::STAGE);
+        const uint32_t b = a + C::A_BYTES;
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t da = tile_desc(a, kk, g.a_mn), db = tile_desc(b, kk, g.b_mn);
-            mma_bf16(dt, da, db, idesc, (kb > kb0 || kk) ? 1u : 0u);
-            if (SPLIT) {
-              const uint64_t dal = tile_desc(a + C::A_BYTES + C::B_BYTES, kk, g.a_mn);
-              const uint64_t dbl = tile_desc(a + 2 * C::A_BYTES + C::B_BYTES, kk, g.b_mn);
-              mma_bf16(dt, da, dbl, idesc, 1u);
-              mma_bf16(dt, dal, db, idesc, 1u);
-            }
-          }
-          mma_commit(&empty[s]);
-          if (++s == C::STAGES) {
-            s = 0;
-            ph ^= 1u;
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          const uint64_t da = tile_desc(a, kk, g.a_mn), db = tile_desc(b, kk, g.b_mn);
+          mma_bf16_w(dt, da, db, idesc, (kb > kb0 || kk) ? 1u : 0u);
+          if (SPLIT) {
+            const uint64_t dal = tile_desc(a + C::A_BYTES + C::B_BYTES, kk, g.a_mn);
+            const uint64_t dbl = tile_desc(a + 2 * C::A_BYTES + C::B_BYTES, kk, g.b_mn);
+            mma_bf16_w(dt, da, dbl, idesc, 1u);
+            mma_bf16_w(dt, dal, db, idesc, 1u);
           }
         }
-        if (!ok) break;
-        mma_commit(&tfull[buf]);
+        mma_commit_w(&empty[s]);
+        if (++s == C::STAGES) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
-      mma_commit(drain);  // every MMA issued above has finished once this arrives
-      wait_drain(drain, 0, g.err);
+      if (!ok) break;
+      mma_commit_w(&tfull[buf]);
     }
+    mma_commit_w(drain);  // every MMA issued above has finished once this arrives
+    wait_drain(drain, 0, g.err);
   } else {  // ------------------------------------------------------------ epilogue
     const int q = warp & 3;             // TMEM lane quadrant this warp may access
     const int half = (warp - 2) >> 2;   // the two warps of a quadrant take alternate column chunks
