@@ -146,7 +146,8 @@ def replica_tokens_per_s(world, steps, tokens_per_step, seconds):
 # DRAM bytes (read + write) of one steady-state launch (window full) of the attention
 # forward at the 760M shape, from `ncu --set full` captures (profiles/attn_fwd_760m.md):
 # the frozen-block pass over 4096 queries, and a trainable block over one 1024-token chunk.
-ATTN_FWD_TRAFFIC_760M = {"pass": 88.29e6 + 5.54e6, "step": 59.84e6 + 1.00e6}
+# None until the current forward kernel has been captured.
+ATTN_FWD_TRAFFIC_760M = None
 
 
 def attn_fwd_traffic(shape, nc):

@@ -270,9 +270,9 @@ __global__ void __launch_bounds__(kF5Threads, 1)
       float m8[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) m8[e] = -INFINITY;
-      if (full) {
+      if (full) {  // eight chains of three-input max
 #pragma unroll
-        for (int e = 0; e < 128; ++e) m8[e & 7] = fmaxf(m8[e & 7], sv[e]);
+        for (int e = 0; e < 64; ++e) m8[e & 7] = fmax3(m8[e & 7], sv[2 * e], sv[2 * e + 1]);
       } else {
 #pragma unroll
         for (int e = 0; e < 128; ++e) {
@@ -289,21 +289,30 @@ __global__ void __launch_bounds__(kF5Threads, 1)
       const float m_use = (m_used == -INFINITY) ? 0.f : m_used;
       // P_j as bf16 pairs over the first 64 columns of S_w (keys 2q, 2q+1 in column q);
       // every score is already in registers
-      float r8[8];
+      // exp2(s * scale - m) on packed pairs: one fma.f32x2, two ex2, one add.f32x2 into
+      // four packed row-sum chains, one bf16x2 conversion per pair of keys
+      const uint64_t sc2 = f32x2(sl2, sl2), nm2 = f32x2(-m_use, -m_use);
+      uint64_t r4[4];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) r8[e] = 0.f;
+      for (int e = 0; e < 4; ++e) r4[e] = f32x2(0.f, 0.f);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t u[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float x0 = ex2_approx(fmaf(sv[32 * c + 2 * e], sl2, -m_use));
-          const float x1 = ex2_approx(fmaf(sv[32 * c + 2 * e + 1], sl2, -m_use));
-          r8[(2 * e) & 7] += x0;
-          r8[(2 * e + 1) & 7] += x1;
+          const float2 y = f32x2_split(ffma2(f32x2(sv[32 * c + 2 * e], sv[32 * c + 2 * e + 1]), sc2, nm2));
+          const float x0 = ex2_approx(y.x), x1 = ex2_approx(y.y);
+          r4[e & 3] = fadd2(r4[e & 3], f32x2(x0, x1));
           u[e] = pack_bf16(x0, x1);
         }
         tmem_st16(tS + (uint32_t)(c * 16), u);
+      }
+      float r8[8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 v = f32x2_split(r4[e]);
+        r8[2 * e] = v.x;
+        r8[2 * e + 1] = v.y;
       }
       if (__any_sync(0xffffffffu, grow) && t > 0) {
         // O_w holds every product of this warpgroup's earlier tiles: S_j was issued after
