@@ -145,7 +145,7 @@ def replica_tokens_per_s(world, steps, tokens_per_step, seconds):
 
 # DRAM bytes (read + write) of one steady-state launch (window full) of the attention
 # forward at the 760M shape, from `ncu --set full` captures (profiles/attn_fwd_760m.md):
-# the frozen-block pass over 4096 queries, and a trainable block over one 1024-token chunk.
+# the frozen-block pass over 8192 queries, and a trainable block over one 1024-token chunk.
 # None until the current forward kernel has been captured.
 ATTN_FWD_TRAFFIC_760M = None
 
@@ -158,7 +158,7 @@ def attn_fwd_traffic(shape, nc):
         return None
     if (shape.n_layers, shape.d_model, shape.window, shape.chunk) != (24, 1536, 8192, 1024):
         return None
-    G = max(1, min(4096 // shape.chunk, shape.window // shape.chunk))
+    G = max(1, min(8192 // shape.chunk, shape.window // shape.chunk))
     passes = -(-nc // G) * (shape.n_layers - shape.n_trainable)
     steps = nc * shape.n_trainable
     t = ATTN_FWD_TRAFFIC_760M

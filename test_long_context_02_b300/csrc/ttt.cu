@@ -108,7 +108,7 @@ using ProfRec = ttt_ctx::ProfRec;
 namespace {
 
 // Rows of one frozen-prefix pass (whole chunks): large enough for full GEMM waves.
-constexpr int kPrefixRows = 4096;
+constexpr int kPrefixRows = 8192;
 
 int fail(ttt_ctx* c, int code, const std::string& msg) {
   if (c) c->err = msg;
