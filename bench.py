@@ -146,8 +146,7 @@ def replica_tokens_per_s(world, steps, tokens_per_step, seconds):
 # DRAM bytes (read + write) of one steady-state launch (window full) of the attention
 # forward at the 760M shape, from `ncu --set full` captures (profiles/attn_fwd_760m.md):
 # the frozen-block pass over 8192 queries, and a trainable block over one 1024-token chunk.
-# None until the current forward kernel has been captured.
-ATTN_FWD_TRAFFIC_760M = None
+ATTN_FWD_TRAFFIC_760M = {"pass": 126.13e6 + 14.71e6, "step": 59.84e6 + 0.81e6}
 
 
 def attn_fwd_traffic(shape, nc):
