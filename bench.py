@@ -109,6 +109,9 @@ class Clocks:
                 "samples": len(sm), "power_w_max": max(pw) if pw else None}
 
 
+_UNPACKED = {}
+
+
 def cpu_sample(shape, blob, tokens, n_tok):
     """Time the oracle on the first n_tok tokens (one inner-loop step) on the host cores."""
     from oracle import ttt_oracle as O
@@ -118,7 +121,11 @@ def cpu_sample(shape, blob, tokens, n_tok):
     except Exception:
         cores = os.cpu_count()
     cfg = O.Config.from_shape(shape.replace(chunk=n_tok))
-    P = O.unpack(blob, cfg)
+    key = (id(blob), n_tok)
+    if key not in _UNPACKED:  # float64 parameters, converted once per process (untimed)
+        _UNPACKED.clear()
+        _UNPACKED[key] = O.unpack(blob, cfg)
+    P = _UNPACKED[key]
     ids = np.asarray(tokens[:n_tok])
     tgt = O.chunk_targets(tokens, 0, n_tok)
     t0 = time.perf_counter()
@@ -169,13 +176,24 @@ def workload_name(s):
             f"theta{s.rope_theta:g} eta{s.eta:g} {s.compute}: {s.n_seqs} x {s.seq_len} tokens")
 
 
+def reference_tokens(steps, warmup, budget_s=120.0, s_per_token=0.025):
+    """Tokens per oracle sample so that steps + warmup samples take about budget_s on the
+    host cores (the float64 oracle runs the 760M shape at about s_per_token per token):
+    a power of two between 64 and 1024, the workload's chunk."""
+    n = budget_s / s_per_token / max(1, steps + warmup)
+    t = 64
+    while t * 2 <= min(n, 1024):
+        t *= 2
+    return t
+
+
 def run_reference(a):
     if int(os.environ.get("RANK", "0")) != 0:
         return 0
     shape = SHAPES[a.workload]
     tokens = sequence_tokens(shape, 0)
     blob = weight_blob(shape)
-    n_tok = a.cpu_tokens
+    n_tok = a.cpu_tokens or reference_tokens(a.steps, a.warmup)
     for _ in range(a.warmup):
         cpu_sample(shape, blob, tokens, n_tok)
     secs, cores = [], None
@@ -332,9 +350,10 @@ def run_ours(a):
                    "d2h_bytes_per_step": 4 * nc, "api": "ttt_prefill_chunk per chunk, pinned host buffers"},
            "final_chunk_loss": float(losses[-1])}
     if world == 1 and not a.no_cpu_baseline:
-        v, cores, dt = cpu_sample(shape, blob, tokens, a.cpu_tokens)
+        n_tok = a.cpu_tokens or 512
+        v, cores, dt = cpu_sample(shape, blob, tokens, n_tok)
         out["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
-                               "sample": f"first {a.cpu_tokens} tokens as one inner-loop step, {dt:.1f} s"}
+                               "sample": f"first {n_tok} tokens as one inner-loop step, {dt:.1f} s"}
     print(json.dumps(out), flush=True)
     m.close()
     if dist is not None:
@@ -350,7 +369,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="760m", choices=sorted(SHAPES))
     ap.add_argument("--tokens", type=int, default=0, help="override the sequence length (smoke runs)")
-    ap.add_argument("--cpu-tokens", type=int, default=128, help="oracle sample size (tokens)")
+    ap.add_argument("--cpu-tokens", type=int, default=None,
+                    help="oracle sample size in tokens (default: 512 for cpu_baseline; for --impl reference, "
+                         "sized so that warm-up and timed samples together take about two minutes)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     a = ap.parse_args()
     if a.warmup < 3:
