@@ -20,6 +20,10 @@
  * Ownership: the context owns all device memory.  Host pointers passed in are
  * read or written only during the call and never retained.
  * Streams: all work is enqueued on the stream given to ttt_create.
+ * Devices and threads: one process drives one GPU.  The library caches launch
+ * settings (per-kernel shared-memory limits, the SM count) on first use, so
+ * every context of a process must live on the same device, and calls that
+ * launch work must not run concurrently from several host threads.
  * Errors: every call returns 0 or a negative TTT_ERR_* code; after an error the
  * context may only be reloaded (ttt_load_weights) or destroyed.
  */
