@@ -105,6 +105,21 @@ TTT_API int ttt_k_attn_rowdot(int n, int H, int dh, const void* do_hi, const voi
                               const void* o_lo, float* D, void* stream);
 
 /*
+ * Failure detection, exercised without a fault: one CTA in which two threads
+ * wait on an mbarrier phase that nothing completes, through the bounded wait
+ * every kernel of the library uses.  Thread 0 of warp 0 starts at once, thread
+ * 0 of warp 1 100 ms later.  After the wait limit (4 s) warp 0's wait gives up:
+ * it raises the CTA abort flag and writes 3 (an epilogue-side wait ran out)
+ * into *err if *err was 0; warp 1's wait then stops at its next check of the
+ * flag, without writing *err.  status[2w] = 1 if warp w's wait succeeded (never)
+ * else 0; status[2w+1] = milliseconds warp w waited.  err and status (4 ints)
+ * are caller-owned DEVICE memory.  Returns TTT_ERR_ARG for a null pointer,
+ * TTT_ERR_CUDA if the launch fails, else 0; the kernel runs about 4 s, and the
+ * context stays usable afterwards.
+ */
+TTT_API int ttt_k_wait_limit_probe(int32_t* err, int32_t* status, void* stream);
+
+/*
  * LM-head cross-entropy statistics WITHOUT ANY DEVICE ALLOCATION.  The paper
  * has no counterpart: this entry point exists for callers that cannot call
  * cudaMalloc, for example a process whose device memory is owned up front by

@@ -113,6 +113,9 @@ ttt_k_attn_rowdot = _sig("ttt_k_attn_rowdot", ctypes.c_int, ctypes.c_int, ctypes
 ttt_k_lmhead_ce_static = _sig("ttt_k_lmhead_ce_static", ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                               _vp, _i64, _vp, _i64, _vp, _vp, _vp, _vp, _vp)
 
+# A bounded wait that runs out on purpose (failure detection without a fault).
+ttt_k_wait_limit_probe = _sig("ttt_k_wait_limit_probe", ctypes.c_int, _vp, _vp, _vp)
+
 ttt_create = _sig("ttt_create", ctypes.c_int, ctypes.POINTER(ttt_config), _vp, ctypes.POINTER(_vp))
 ttt_load_weights = _sig("ttt_load_weights", ctypes.c_int, _vp, _vp, ctypes.c_size_t)
 ttt_prefill_chunk = _sig("ttt_prefill_chunk", ctypes.c_int, _vp, _vp, _i32, _vp, _vp)
@@ -173,6 +176,11 @@ def attn_bwd(n, H, dh, window, pos0, q, kc, vc, ko, vo, do, lse, D, dq, dk, dv, 
 def attn_rowdot(n, H, dh, do, o, D, *, do_lo=None, o_lo=None, stream=None):
     return check(ttt_k_attn_rowdot(n, H, dh, ptr(do), ptr(do_lo), ptr(o), ptr(o_lo), ptr(D), _stream(stream)),
                  "ttt_k_attn_rowdot")
+
+
+def wait_limit_probe(err, status, *, stream=None):
+    """ttt_k_wait_limit_probe: err [1] and status [4] int32 device tensors."""
+    return check(ttt_k_wait_limit_probe(ptr(err), ptr(status), _stream(stream)), "ttt_k_wait_limit_probe")
 
 
 def lmhead_ce_static(M, K, V, x, w_lm, tgt, lse, loss, *, ldx=None, ldw=None, err=None, stream=None):
