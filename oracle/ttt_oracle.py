@@ -47,7 +47,7 @@ __all__ = ["Config", "unpack", "pack", "rmsnorm", "rmsnorm_bwd", "rope_angles",
            "rope", "rope_bwd", "gelu_tanh", "gelu_tanh_grad", "attention",
            "attention_bwd", "cross_entropy", "init_state", "chunk_forward",
            "chunk_backward", "ttt_step", "run_sequence", "dense_forward_losses",
-           "trainable_names"]
+           "trainable_names", "decode", "greedy", "sampler"]
 
 
 @dataclass(frozen=True)
@@ -418,3 +418,102 @@ def dense_forward_losses(cfg: Config, P: dict, tokens, chunk=None):
         seg = seg[~np.isnan(seg)]
         out.append(float(seg.mean()) if seg.size else 0.0)
     return out
+
+
+# ----------------------------------------------------------------------------
+# decode-phase TTT
+# ----------------------------------------------------------------------------
+def greedy(z_row, i):
+    """Pick the first index of the largest logit (the i-th generated token)."""
+    return int(np.argmax(z_row))
+
+
+def sampler(u, temp):
+    """Pick the i-th generated token from softmax(z / temp) by inverse CDF at the
+    caller's uniform u[i] in [0, 1): the first index whose cumulative weight
+    exceeds u[i] times the total."""
+    def pick(z_row, i):
+        y = np.asarray(z_row, np.float64) / temp
+        c = np.cumsum(np.exp(y - y.max()))
+        return int(np.searchsorted(c, u[i] * c[-1], side="right"))
+    return pick
+
+
+def decode(cfg: Config, P: dict, prompt, n_new, eta, pick, trace=False):
+    """Decode-phase TTT: prefill the prompt with the chunked inner loop, then
+    generate n_new tokens, taking one inner-loop step after every chunk of b
+    generated tokens (pages: "TTT-E2E技术：突破大语言模型上下文限制的新范式", §2.2
+    "批量更新与稳定性控制", one update per 1000 input tokens while prefilling and one
+    per 1000 output tokens while generating; "把 Transformer 做成“终身学习者”", §4.2,
+    the inner loop reused at inference).
+
+    Readings where the pages are silent:
+      * the prompt goes through the chunked inner loop exactly as run_sequence
+        does; its last position has no target;
+      * the token at position t is picked from the logits of position t - 1, as
+        computed by the forward of t - 1's chunk (before that chunk's update); the
+        first generated token comes from the prompt's last position;
+      * generated tokens form chunks of b starting at the first generated
+        position; a complete chunk takes one step (forward, mean next-token
+        cross-entropy over its b positions, suffix backward, SGD, cache commit),
+        and its last position's target is the token picked after it, from the
+        logits of that position before the update; an incomplete last chunk
+        takes no step;
+      * pick(z_row, i) chooses the i-th generated token (i = 0 for the first);
+        random numbers, if any, are the caller's (see sampler).
+
+    Returns a dict: tokens (the n_new generated ids), next (the id picked after
+    them), prefill_losses, gen_losses, P (final parameters), state, and with
+    trace=True, hist: the fast weights after every step, prompt chunks first,
+    and z: the logits row behind every pick (n_new + 1 rows).
+    """
+    b = cfg.chunk
+    prompt = np.asarray(prompt)
+    T = len(prompt)
+    if T < 1:
+        raise ValueError("decode needs a prompt of at least one token")
+    state = init_state(cfg)
+    names = trainable_names(cfg)
+    hist, pre_losses, gen_losses = [], [], []
+
+    def step(P, state, ids, tgt):
+        z, saved, new_kv = chunk_forward(cfg, P, state, ids)
+        loss = chunk_loss(z, tgt)
+        grads = chunk_backward(cfg, P, saved, z, tgt)
+        P2 = dict(P)
+        for name, g in grads.items():
+            P2[name] = P[name] - eta * g
+        if trace:
+            hist.append({k: P2[k].copy() for k in names})
+        return loss, P2, _commit(cfg, state, new_kv, len(ids)), z
+
+    z_last = None
+    for s in range(0, T, b):
+        n = min(b, T - s)
+        loss, P, state, z = step(P, state, prompt[s:s + n], chunk_targets(prompt, s, n))
+        pre_losses.append(loss)
+        z_last = z[-1]
+
+    out, cur, rows = [], [], []
+
+    def pick_from(z_row, i):
+        rows.append(z_row)
+        return pick(z_row, i)
+
+    nxt = pick_from(z_last, 0)
+    for i in range(n_new):
+        out.append(nxt)
+        cur.append(nxt)
+        # the current chunk so far, with its starting weights: the row of the newest token
+        z, _, _ = chunk_forward(cfg, P, state, np.asarray(cur), keep=False)
+        nxt = pick_from(z[-1], i + 1)
+        if len(cur) == b:
+            ids = np.asarray(cur)
+            loss, P, state, _ = step(P, state, ids, np.append(ids[1:], nxt))
+            gen_losses.append(loss)
+            cur = []
+    res = dict(tokens=out, next=nxt, prefill_losses=pre_losses, gen_losses=gen_losses, P=P, state=state)
+    if trace:
+        res["hist"] = hist
+        res["z"] = np.stack(rows)
+    return res
