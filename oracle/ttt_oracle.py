@@ -25,6 +25,11 @@ What it computes (pages: "把 Transformer 做成“终身学习者”：TTT-E2E 
 Model (pre-norm, row-vector convention y = x.W, no biases, untied LM head):
     h = x + Attn(RMSNorm_a(x));   y = h + GELU_tanh(RMSNorm_m(h).W_up).W_down
     logits = RMSNorm_f(x_L).W_lm
+Dual-MLP variant (Config.dual_mlp; "从KV Cache到权重压缩：大模型持续学习的新范式", §2.2,
+a static MLP that keeps the pretrained knowledge beside a dynamic one that
+adapts): in the trainable blocks
+    y = h + GELU_tanh(n.W_up).W_down + GELU_tanh(n.W_up_s).W_down_s,  n = RMSNorm_m(h),
+where only W_up, W_down are fast weights and the static pair stays frozen.
 RMSNorm eps 1e-6, gains 1 unless loaded; RoPE rotate-half, inv_freq_i =
 theta^(-2i/d_head), absolute 0-based positions; attention scale 1/sqrt(d_head);
 a query at position p sees keys j with p - k < j <= p.
@@ -61,6 +66,8 @@ class Config:
     chunk: int
     rope_theta: float
     rms_eps: float = 1e-6
+    # dual-MLP variant: each trainable block adds a frozen static MLP beside the fast one
+    dual_mlp: bool = False
 
     @property
     def n_trainable(self) -> int:
@@ -74,7 +81,7 @@ class Config:
     @staticmethod
     def from_shape(s) -> "Config":
         return Config(s.n_layers, s.d_model, s.n_heads, s.d_ff, s.vocab,
-                      s.window, s.chunk, s.rope_theta, s.rms_eps)
+                      s.window, s.chunk, s.rope_theta, s.rms_eps, getattr(s, "dual_mlp", False))
 
 
 # ----------------------------------------------------------------------------
@@ -88,6 +95,8 @@ def _layout(cfg: Config):
         out += [(f"g_attn.{l}", (d,)), (f"Wq.{l}", (d, d)), (f"Wk.{l}", (d, d)),
                 (f"Wv.{l}", (d, d)), (f"Wo.{l}", (d, d)), (f"g_mlp.{l}", (d,)),
                 (f"W_up.{l}", (d, f)), (f"W_down.{l}", (f, d))]
+        if cfg.dual_mlp and l >= cfg.n_layers - cfg.n_trainable:
+            out += [(f"W_up_s.{l}", (d, f)), (f"W_down_s.{l}", (f, d))]
     return out + [("g_final", (d,)), ("W_lm", (d, V))]
 
 
@@ -278,9 +287,13 @@ def chunk_forward(cfg: Config, P: dict, state, ids, keep=True):
         a = xn_m @ P[f"W_up.{l}"]
         u = gelu_tanh(a)
         y = h + u @ P[f"W_down.{l}"]
+        a_s = None
+        if cfg.dual_mlp and l >= L - cfg.n_trainable:   # static MLP on the same normalised input
+            a_s = xn_m @ P[f"W_up_s.{l}"]
+            y = y + gelu_tanh(a_s) @ P[f"W_down_s.{l}"]
         if keep and l >= L - cfg.n_trainable:
             acts.append(dict(x=x, r_a=r_a, q=q, kall=kall, vall=vall, pall=pall,
-                             h=h, xn_m=xn_m, r_m=r_m, a=a, u=u))
+                             h=h, xn_m=xn_m, r_m=r_m, a=a, u=u, a_s=a_s))
         else:
             acts.append(None)
         new_kv.append((k, v))
@@ -313,7 +326,10 @@ def chunk_backward(cfg: Config, P: dict, saved, z, tgt):
         grads[f"W_up.{l}"] = A["xn_m"].T @ da
         if l == L - S:
             break       # the first trainable block's attention needs no backward
-        dh = dy + rmsnorm_bwd(da @ P[f"W_up.{l}"].T, A["h"], P[f"g_mlp.{l}"], A["r_m"])
+        dxn_m = da @ P[f"W_up.{l}"].T
+        if A["a_s"] is not None:   # the static MLP passes gradient to h; its weights stay frozen
+            dxn_m = dxn_m + ((dy @ P[f"W_down_s.{l}"].T) * gelu_tanh_grad(A["a_s"])) @ P[f"W_up_s.{l}"].T
+        dh = dy + rmsnorm_bwd(dxn_m, A["h"], P[f"g_mlp.{l}"], A["r_m"])
         do = _heads(dh @ P[f"Wo.{l}"].T, H)
         dq, dk, dv = attention_bwd(do, A["q"], A["kall"], A["vall"], pos, A["pall"],
                                    cfg.window)
@@ -409,7 +425,10 @@ def dense_forward_losses(cfg: Config, P: dict, tokens, chunk=None):
         o, _ = attention(q, k, v, pos, pos, cfg.window)
         h = x + _merge(o) @ P[f"Wo.{l}"]
         xn_m, _ = rmsnorm(h, P[f"g_mlp.{l}"], cfg.rms_eps)
-        x = h + gelu_tanh(xn_m @ P[f"W_up.{l}"]) @ P[f"W_down.{l}"]
+        y = h + gelu_tanh(xn_m @ P[f"W_up.{l}"]) @ P[f"W_down.{l}"]
+        if cfg.dual_mlp and l >= cfg.n_layers - cfg.n_trainable:
+            y = y + gelu_tanh(xn_m @ P[f"W_up_s.{l}"]) @ P[f"W_down_s.{l}"]
+        x = y
     xf, _ = rmsnorm(x, P["g_final"], cfg.rms_eps)
     loss, _ = cross_entropy(xf @ P["W_lm"], chunk_targets(tokens, 0, T))
     out = []

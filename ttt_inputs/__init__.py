@@ -43,6 +43,7 @@ class Shape:
     n_seqs: int = 1
     compute: str = "bf16"          # "fp32" or "bf16"
     rms_eps: float = 1e-6
+    dual_mlp: bool = False         # trainable blocks carry a frozen static MLP beside the fast one
 
     @property
     def n_trainable(self) -> int:
@@ -77,7 +78,9 @@ def blob_layout(shape: Shape):
     """(name, shape, is_gain) for every tensor of the fp32 weight blob, in order.
 
     Order: E[V][d]; per layer g_attn[d], Wq, Wk, Wv, Wo [d][d], g_mlp[d],
-    W_up[d][f], W_down[f][d]; g_final[d]; W_lm[d][V].  Row-major, y = x.W.
+    W_up[d][f], W_down[f][d] (with dual_mlp, the trainable layers then add the
+    static pair W_up_s[d][f], W_down_s[f][d]); g_final[d]; W_lm[d][V].
+    Row-major, y = x.W.
     """
     d, f, V = shape.d_model, shape.d_ff, shape.vocab
     out = [("E", (V, d), False)]
@@ -87,6 +90,8 @@ def blob_layout(shape: Shape):
                 (f"Wv.{l}", (d, d), False), (f"Wo.{l}", (d, d), False),
                 (f"g_mlp.{l}", (d,), True),
                 (f"W_up.{l}", (d, f), False), (f"W_down.{l}", (f, d), False)]
+        if shape.dual_mlp and l >= shape.n_layers - shape.n_trainable:
+            out += [(f"W_up_s.{l}", (d, f), False), (f"W_down_s.{l}", (f, d), False)]
     out += [("g_final", (d,), True), ("W_lm", (d, V), False)]
     return out
 
