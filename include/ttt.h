@@ -69,6 +69,11 @@ typedef struct {
   int32_t compute;      /* 0: fp32 (every product as three bf16 products of hi/lo
                            halves, fp32 accumulate); 1: bf16 operands, fp32
                            accumulate; fast weights are fp32 in both           */
+  int32_t dual_mlp;     /* 0: one MLP per block.  1: the dual-MLP variant ("从KV Cache到
+                           权重压缩：大模型持续学习的新范式", §2.2): each trainable block
+                           adds a frozen static MLP on the same normalised input,
+                           y = h + GELU(n.W_up).W_down + GELU(n.W_up_s).W_down_s,
+                           n = RMSNorm(h); only W_up, W_down are fast weights   */
 } ttt_config;
 
 /*
@@ -89,6 +94,9 @@ TTT_API int ttt_create(const ttt_config* cfg, void* cuda_stream, ttt_ctx** out);
  *   for each layer: g_attn[d], Wq[d][d], Wk[d][d], Wv[d][d], Wo[d][d],
  *                   g_mlp[d], W_up[d][d_ff], W_down[d_ff][d];
  *   g_final[d]; W_lm[d][V].
+ * With dual_mlp = 1, each trainable layer (the last n_trainable) adds its
+ * static pair W_up_s[d][d_ff], W_down_s[d_ff][d] right after its W_down.
+ * A blob of any other size returns TTT_ERR_ARG.
  */
 TTT_API int ttt_load_weights(ttt_ctx* ctx, const float* host_blob, size_t n_floats);
 
@@ -121,6 +129,16 @@ TTT_API int ttt_prefill_chunk_dev(ttt_ctx* ctx, const int32_t* d_tokens, int32_t
  * last position has none).  Asynchronous like ttt_prefill_chunk_dev.
  */
 TTT_API int ttt_prefill_sequence_dev(ttt_ctx* ctx, const int32_t* d_tokens, int32_t T, float* d_losses);
+
+/*
+ * Whole sequences with HOST buffers: tokens int32 [n_seqs][T] (checked on the
+ * host: ids in [0, vocab)), losses float [n_seqs][ceil(T/b)], out.  The
+ * tokens go to the device in one copy, the sequence runs as in
+ * ttt_prefill_sequence_dev, and the losses come back in one copy; blocks
+ * until they are on the host.  The context keeps a device staging buffer for
+ * the tokens and losses, grown (one cudaMalloc) when a longer T comes in.
+ */
+TTT_API int ttt_prefill_sequence(ttt_ctx* ctx, const int32_t* tokens, int32_t T, float* losses);
 
 /* Wait for the context stream and report a device-side error (TTT_ERR_DEVICE). */
 TTT_API int ttt_sync(ttt_ctx* ctx);

@@ -135,8 +135,11 @@ TTT_API int ttt_k_wait_limit_probe(int32_t* err, int32_t* status, void* stream);
  *
  * Scratch: the partial (max, sum) pairs of every (row, vocab tile) and the
  * target logits live in one file-scope __device__ array of
- * TTT_CE_STATIC_SCRATCH_ENTRIES float2 (4 MiB), held by every GPU that loads
- * the library until the process exits.  Every scratch element a call reads is
+ * TTT_CE_STATIC_SCRATCH_ENTRIES float2 (4 MiB).  The CUDA runtime loads the
+ * library's modules lazily, so the array is allocated on a device by the
+ * first call there (the symbol lookup below loads its module) and is held
+ * until the process exits; a caller whose memory another allocator reserves
+ * up front should make its first call before that reservation.  Every scratch element a call reads is
  * written earlier in the same call, so nothing needs clearing between calls.
  * All calls share that one array: calls whose work overlaps on the GPU (other
  * streams, other host threads) race and give wrong results; serialise them.
@@ -145,7 +148,8 @@ TTT_API int ttt_k_wait_limit_probe(int32_t* err, int32_t* status, void* stream);
  * TTT_ERR_SCRATCH before anything is enqueued.
  * The first call on a device looks up the array's device address with
  * cudaGetSymbolAddress (once per device, with that device current); make that
- * first call before any stream capture.  Returns 0, TTT_ERR_ARG (null
+ * first call before any stream capture.  Like the rest of the library (ttt.h),
+ * one process drives one GPU: launch settings are cached per process.  Returns 0, TTT_ERR_ARG (null
  * pointer, size < 1, pitch < width or not a multiple of 8), TTT_ERR_SCRATCH,
  * or TTT_ERR_CUDA (symbol lookup or launch failure).
  */

@@ -40,7 +40,8 @@ class TTTError(RuntimeError):
 class ttt_config(ctypes.Structure):
     _fields_ = [("n_layers", _i32), ("n_trainable", _i32), ("d_model", _i32), ("n_heads", _i32),
                 ("d_ff", _i32), ("vocab", _i32), ("window", _i32), ("chunk", _i32), ("n_seqs", _i32),
-                ("rope_theta", ctypes.c_double), ("rms_eps", _f32), ("eta", _f32), ("compute", _i32)]
+                ("rope_theta", ctypes.c_double), ("rms_eps", _f32), ("eta", _f32), ("compute", _i32),
+                ("dual_mlp", _i32)]
 
 
 class ttt_gemm_epilogue(ctypes.Structure):
@@ -121,6 +122,7 @@ ttt_load_weights = _sig("ttt_load_weights", ctypes.c_int, _vp, _vp, ctypes.c_siz
 ttt_prefill_chunk = _sig("ttt_prefill_chunk", ctypes.c_int, _vp, _vp, _i32, _vp, _vp)
 ttt_prefill_chunk_dev = _sig("ttt_prefill_chunk_dev", ctypes.c_int, _vp, _vp, _i32, _vp, _vp)
 ttt_prefill_sequence_dev = _sig("ttt_prefill_sequence_dev", ctypes.c_int, _vp, _vp, _i32, _vp)
+ttt_prefill_sequence = _sig("ttt_prefill_sequence", ctypes.c_int, _vp, _vp, _i32, _vp)
 ttt_sync = _sig("ttt_sync", ctypes.c_int, _vp)
 ttt_get_fast_weights = _sig("ttt_get_fast_weights", ctypes.c_int, _vp, _i32, _i32, _vp, _vp)
 ttt_position = _sig("ttt_position", _i64, _vp)
@@ -192,13 +194,14 @@ def lmhead_ce_static(M, K, V, x, w_lm, tgt, lse, loss, *, ldx=None, ldw=None, er
 
 
 def make_config(n_layers, d_model, n_heads, d_ff, vocab, window, chunk, rope_theta, eta, n_seqs=1,
-                compute="bf16", rms_eps=1e-6, n_trainable=None):
+                compute="bf16", rms_eps=1e-6, n_trainable=None, dual_mlp=False):
     c = ttt_config()
     c.n_layers, c.d_model, c.n_heads, c.d_ff, c.vocab = n_layers, d_model, n_heads, d_ff, vocab
     c.n_trainable = n_layers // 4 if n_trainable is None else n_trainable
     c.window, c.chunk, c.n_seqs = window, chunk, n_seqs
     c.rope_theta, c.rms_eps, c.eta = float(rope_theta), float(rms_eps), float(eta)
     c.compute = 0 if compute == "fp32" else 1
+    c.dual_mlp = 1 if dual_mlp else 0
     return c
 
 
@@ -216,7 +219,8 @@ class TTT:
     def from_shape(cls, shape, stream=None, **over):
         kw = dict(n_layers=shape.n_layers, d_model=shape.d_model, n_heads=shape.n_heads, d_ff=shape.d_ff,
                   vocab=shape.vocab, window=shape.window, chunk=shape.chunk, rope_theta=shape.rope_theta,
-                  eta=shape.eta, n_seqs=shape.n_seqs, compute=shape.compute, rms_eps=shape.rms_eps)
+                  eta=shape.eta, n_seqs=shape.n_seqs, compute=shape.compute, rms_eps=shape.rms_eps,
+                  dual_mlp=getattr(shape, "dual_mlp", False))
         kw.update(over)
         return cls(make_config(**kw), stream)
 
@@ -244,6 +248,15 @@ class TTT:
 
     def prefill_sequence_dev(self, d_tokens, T, d_losses):
         self._check(ttt_prefill_sequence_dev(self._h, ptr(d_tokens), T, ptr(d_losses)), "ttt_prefill_sequence_dev")
+
+    def prefill_sequence(self, tokens) -> np.ndarray:
+        """Whole sequences from host memory: tokens [n_seqs][T] -> chunk losses [n_seqs][ceil(T/b)]."""
+        tokens = np.ascontiguousarray(tokens, np.int32).reshape(self.cfg.n_seqs, -1)
+        Tn = tokens.shape[1]
+        losses = np.zeros((self.cfg.n_seqs, -(-Tn // self.cfg.chunk)), np.float32)
+        self._check(ttt_prefill_sequence(self._h, tokens.ctypes.data, Tn, losses.ctypes.data),
+                    "ttt_prefill_sequence")
+        return losses
 
     def sync(self):
         self._check(ttt_sync(self._h), "ttt_sync")

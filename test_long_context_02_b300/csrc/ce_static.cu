@@ -18,8 +18,9 @@ using namespace ttt;
 namespace {
 
 // 4 MiB: (max, sum) pairs for M rows x ceil(V / tile) vocab tiles, then M
-// target logits packed two per entry.  Every device that loads the library
-// holds this array until the process exits.
+// target logits packed two per entry.  Module loading is lazy, so a device
+// allocates the array when the first call there looks up its address, and
+// holds it until the process exits.
 constexpr long kScratchEntries = TTT_CE_STATIC_SCRATCH_ENTRIES;
 static __device__ __align__(256) float2 g_ce_scratch[kScratchEntries];
 

@@ -9,10 +9,12 @@
 // “终身学习者”", §4.2, one mini-batch gradient step on the last-quarter MLPs;
 // "测试时训练：长上下文的持续学习", §2.1.2, theta <- theta - eta*grad).
 //
-// CTA = 6 warps: warp 0 issues TMA loads into a ring of shared-memory stages,
-// warp 1 owns the TMEM accumulators and issues tcgen05.mma (single thread),
-// warps 2-5 drain a 128 x BN fp32 accumulator from TMEM (one row per thread)
-// and apply the epilogue while the MMA warp fills the other accumulator.
+// CTA = 10 warps: warp 0 issues TMA loads into a ring of shared-memory stages;
+// warp 1 owns the TMEM accumulators and issues tcgen05.mma (the whole warp
+// runs the loop, one lane chosen by elect.sync issues); warps 2-9 drain a
+// 128 x BN fp32 accumulator from TMEM, two warps per 32-lane quadrant taking
+// alternate 32-column chunks, and apply the epilogue while the MMA warp fills
+// the other accumulator.
 // Tiles are 128 x BN x 64 (bf16, 128-byte swizzle); operands are K-major or
 // MN-major per call, so weights stay in one row-major copy for both x.W
 // (MN-major B) and dY.W^T (K-major B), and dW = X^T dY reads activations

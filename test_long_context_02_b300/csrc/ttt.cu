@@ -58,7 +58,7 @@ struct Seq {
 struct ttt_ctx {
   ttt_config cfg{};
   cudaStream_t st = nullptr;
-  bool split = false, loaded = false;
+  bool split = false, loaded = false, dual = false;
   std::string err;
   int L = 0, S = 0, d = 0, H = 0, dh = 0, f = 0, V = 0, k = 0, b = 0, B = 0;
   int G = 1, R = 0;  // chunks per frozen-prefix pass, and its rows G*b
@@ -67,6 +67,7 @@ struct ttt_ctx {
   float* E = nullptr;        // [V][d]
   float* gains = nullptr;    // [2L+1][d]: g_attn(l), g_mlp(l), g_final
   Pair Wqkv, Wo, Wup, Wdown, Wlm;  // [L][d][3d], [L][d][d], [L-S][d][f], [L-S][f][d], [d][V]
+  Pair Wup_s, Wdown_s;             // dual-MLP variant: static pair of the trainable blocks [S][d][f], [S][f][d]
   std::vector<Seq> seqs;
   // per-step device scratch
   int *tok = nullptr, *tgt = nullptr, *next = nullptr, *minus1 = nullptr, *derr = nullptr;
@@ -83,6 +84,12 @@ struct ttt_ctx {
   float2* part = nullptr;
   float *dy = nullptr, *dxn = nullptr, *dh32 = nullptr, *D = nullptr, *dq = nullptr, *dk = nullptr, *dv = nullptr;
   Pair dy16, da, dh16, do16, dqkv;
+  float* sa_s = nullptr;     // dual-MLP: static pre-activations [S][b][f]
+  Pair us, da_s;             // dual-MLP: static GELU output and its gradient [b][f]
+  // host whole-sequence entry point: device staging of tokens and losses (grown on demand)
+  int* seq_tok = nullptr;
+  float* seq_loss = nullptr;
+  size_t seq_tok_cap = 0, seq_loss_cap = 0;
   // initial fast weights (device copy) for ttt_reset
   float *init_up = nullptr, *init_down = nullptr;
   // launch counting and optional per-class event timing
@@ -309,6 +316,19 @@ int layer_forward(ttt_ctx* c, Seq& sq_, int l, int si, int n, long pos0, float* 
     RUN(K_GEMM_DOWN, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 0,
         gemm_run(EPI_RESID, opnd(ub, f, 0), opnd(w, d, 1), g, sp, st));
   }
+  if (suf && c->dual) {  // the frozen static MLP of a trainable block, on the same normalised input
+    GemmArgs g;
+    g.M = n; g.N = f; g.K = d;
+    g.out32 = c->sa_s + (long)si * b * f; g.ldo32 = f; g.oh = c->us.hi; g.ol = c->us.lo; g.ldo = f;
+    g.err = c->derr;
+    RUN(K_GEMM_UP, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 0,
+        gemm_run(EPI_GELU, opnd(xn_m, d, 0), opnd(c->Wup_s.at((long)si * d * f), f, 1), g, sp, st));
+    GemmArgs g2;  // y += u_s . W_down_s, in place over the block output
+    g2.M = n; g2.N = d; g2.K = f;
+    g2.out32 = xout; g2.ldo32 = d; g2.resid = xout; g2.ldr = d; g2.err = c->derr; g2.allow_ksplit = true;
+    RUN(K_GEMM_DOWN, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 0,
+        gemm_run(EPI_RESID, opnd(c->us, f, 0), opnd(c->Wdown_s.at((long)si * f * d), d, 1), g2, sp, st));
+  }
   return TTT_OK;
 }
 
@@ -437,6 +457,19 @@ int suffix_step(ttt_ctx* c, int s, int row, const int* tok, int n, const int* ne
       RUN(K_MLP_DX, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 0,
           gemm_run(EPI_F32, opnd(c->da, f, 0), opnd(up16, f, 0), g, sp, st));
     }
+    if (si > 0 && c->dual) {  // the static MLP passes gradient to its input: dXn_m += dA_s W_up_s^T
+      GemmArgs g;
+      g.M = n; g.N = f; g.K = d;
+      g.aux = c->sa_s + (long)si * b * f; g.ldaux = f;
+      g.oh = c->da_s.hi; g.ol = c->da_s.lo; g.ldo = f; g.err = c->derr;
+      RUN(K_MLP_DX, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 0,
+          gemm_run(EPI_GELU_BWD, opnd(c->dy16, d, 0), opnd(c->Wdown_s.at((long)si * f * d), d, 0), g, sp, st));
+      GemmArgs g2;
+      g2.M = n; g2.N = d; g2.K = f;
+      g2.out32 = c->dxn; g2.ldo32 = d; g2.resid = c->dxn; g2.ldr = d; g2.err = c->derr; g2.allow_ksplit = true;
+      RUN(K_MLP_DX, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 0,
+          gemm_run(EPI_RESID, opnd(c->da_s, f, 0), opnd(c->Wup_s.at((long)si * d * f), f, 0), g2, sp, st));
+    }
     {  // W_up -= eta Xn_m^T dA
       GemmArgs g;
       g.M = d; g.N = f; g.K = n;
@@ -526,7 +559,8 @@ extern "C" int ttt_create(const ttt_config* cfg, void* cuda_stream, ttt_ctx** ou
   const ttt_config& g = *cfg;
   if (g.n_layers <= 0 || g.n_trainable <= 0 || g.n_trainable > g.n_layers || g.d_model <= 0 || g.n_heads <= 0 ||
       g.d_ff <= 0 || g.vocab <= 0 || g.window <= 0 || g.chunk <= 0 || g.n_seqs <= 0 || g.chunk > g.window ||
-      g.d_model % g.n_heads != 0 || !(g.rope_theta > 0) || !(g.rms_eps >= 0) || (g.compute != 0 && g.compute != 1))
+      g.d_model % g.n_heads != 0 || !(g.rope_theta > 0) || !(g.rms_eps >= 0) || (g.compute != 0 && g.compute != 1) ||
+      (g.dual_mlp != 0 && g.dual_mlp != 1))
     return TTT_ERR_ARG;
   const int dh = g.d_model / g.n_heads;
   const bool split = g.compute == 0;
@@ -537,6 +571,7 @@ extern "C" int ttt_create(const ttt_config* cfg, void* cuda_stream, ttt_ctx** ou
   c->cfg = g;
   c->st = (cudaStream_t)cuda_stream;
   c->split = split;
+  c->dual = g.dual_mlp == 1;
   c->L = g.n_layers; c->S = g.n_trainable; c->d = g.d_model; c->H = g.n_heads; c->dh = dh; c->f = g.d_ff;
   c->V = g.vocab; c->k = g.window; c->b = g.chunk; c->B = g.n_seqs;
   // the frozen blocks run ahead over up to kPrefixRows tokens of whole chunks, never more than the window
@@ -551,6 +586,10 @@ extern "C" int ttt_create(const ttt_config* cfg, void* cuda_stream, ttt_ctx** ou
   c->Wup = palloc(c, (L - S) * d * f, ok);
   c->Wdown = palloc(c, (L - S) * f * d, ok);
   c->Wlm = palloc(c, d * V, ok);
+  if (c->dual) {
+    c->Wup_s = palloc(c, S * d * f, ok);
+    c->Wdown_s = palloc(c, S * f * d, ok);
+  }
   c->seqs.resize(g.n_seqs);
   for (auto& s : c->seqs) {
     s.ring_k = palloc(c, L * k * d, ok);
@@ -612,6 +651,11 @@ extern "C" int ttt_create(const ttt_config* cfg, void* cuda_stream, ttt_ctx** ou
   c->dh16 = palloc(c, b * d, ok);
   c->do16 = palloc(c, b * d, ok);
   c->dqkv = palloc(c, b * 3 * d, ok);
+  if (c->dual) {
+    c->sa_s = dalloc<float>(c, S * b * f, ok);
+    c->us = palloc(c, b * f, ok);
+    c->da_s = palloc(c, b * f, ok);
+  }
   if (!ok) {
     ttt_destroy(c);
     return TTT_ERR_OOM;
@@ -634,6 +678,8 @@ extern "C" void ttt_destroy(ttt_ctx* c) {
   if (c->st) cudaStreamSynchronize(c->st);
   cudaDeviceSynchronize();
   for (void* p : c->allocs) cudaFree(p);
+  if (c->seq_tok) cudaFree(c->seq_tok);
+  if (c->seq_loss) cudaFree(c->seq_loss);
   for (cudaEvent_t e : c->ev_pool) cudaEventDestroy(e);
   delete c;
 }
@@ -645,7 +691,8 @@ extern "C" int64_t ttt_position(const ttt_ctx* c) { return (c && !c->seqs.empty(
 extern "C" int ttt_load_weights(ttt_ctx* c, const float* blob, size_t n_floats) {
   if (!c || !blob) return TTT_ERR_ARG;
   const long L = c->L, S = c->S, d = c->d, f = c->f, V = c->V;
-  const size_t need = (size_t)(V * d + L * (2 * d + 4 * d * d + 2 * d * f) + d + d * V);
+  const size_t need = (size_t)(V * d + L * (2 * d + 4 * d * d + 2 * d * f) + d + d * V) +
+                      (c->dual ? (size_t)(S * 2 * d * f) : 0);
   if (n_floats != need) return fail(c, TTT_ERR_ARG, "blob size " + std::to_string(n_floats) + " != " + std::to_string(need));
   c->loaded = false;
   cudaStream_t st = c->st;
@@ -689,6 +736,12 @@ extern "C" int ttt_load_weights(ttt_ctx* c, const float* blob, size_t n_floats) 
           Pair wu = s.up16.at(si * d * f), wd = s.down16.at(si * f * d);
           CK(rows_convert(up, d, (int)f, f, wu.hi, wu.lo, f, st));
           CK(rows_convert(down, f, (int)d, d, wd.hi, wd.lo, d, st));
+        }
+        if (c->dual) {  // the static pair follows the block's W_down
+          Pair su = c->Wup_s.at(si * d * f), sd = c->Wdown_s.at(si * f * d);
+          CK(rows_convert(stage + off, d, (int)f, f, su.hi, su.lo, f, st));
+          CK(rows_convert(stage + off + d * f, f, (int)d, d, sd.hi, sd.lo, d, st));
+          off += 2 * d * f;
         }
       }
     }
@@ -796,6 +849,36 @@ extern "C" int ttt_prefill_sequence_dev(ttt_ctx* c, const int32_t* d_tokens, int
     }
   }
   return TTT_OK;
+}
+
+extern "C" int ttt_prefill_sequence(ttt_ctx* c, const int32_t* tokens, int32_t T, float* losses) {
+  if (!c || !tokens || !losses || T < 1) return TTT_ERR_ARG;
+  if (!c->loaded) return fail(c, TTT_ERR_STATE, "weights not loaded");
+  const size_t ntok = (size_t)c->B * T, nloss = (size_t)c->B * ((T + c->b - 1) / c->b);
+  for (size_t i = 0; i < ntok; ++i)
+    if (tokens[i] < 0 || tokens[i] >= c->V) return fail(c, TTT_ERR_ARG, "token id outside [0, vocab)");
+  if (ntok > c->seq_tok_cap || nloss > c->seq_loss_cap) {  // grow the staging buffers (synchronises)
+    if (cudaStreamSynchronize(c->st) != cudaSuccess) return fail(c, TTT_ERR_CUDA, "stream synchronize");
+    if (c->seq_tok) cudaFree(c->seq_tok);
+    if (c->seq_loss) cudaFree(c->seq_loss);
+    c->seq_tok = nullptr;
+    c->seq_loss = nullptr;
+    c->seq_tok_cap = c->seq_loss_cap = 0;
+    if (cudaMalloc(&c->seq_tok, ntok * sizeof(int32_t)) != cudaSuccess ||
+        cudaMalloc(&c->seq_loss, nloss * sizeof(float)) != cudaSuccess) {
+      cudaGetLastError();
+      return fail(c, TTT_ERR_OOM, "sequence staging buffers");
+    }
+    c->seq_tok_cap = ntok;
+    c->seq_loss_cap = nloss;
+  }
+  if (cudaMemcpyAsync(c->seq_tok, tokens, ntok * sizeof(int32_t), cudaMemcpyHostToDevice, c->st) != cudaSuccess)
+    return fail(c, TTT_ERR_CUDA, "token upload");
+  const int r = ttt_prefill_sequence_dev(c, c->seq_tok, T, c->seq_loss);
+  if (r != TTT_OK) return r;
+  if (cudaMemcpyAsync(losses, c->seq_loss, nloss * sizeof(float), cudaMemcpyDeviceToHost, c->st) != cudaSuccess)
+    return fail(c, TTT_ERR_CUDA, "loss download");
+  return ttt_sync(c);
 }
 
 extern "C" int ttt_get_fast_weights(ttt_ctx* c, int32_t seq, int32_t sl, float* w_up, float* w_down) {

@@ -54,7 +54,7 @@ LAYOUT_PROBE = r"""
 int main(void) {
   printf("ttt_config %zu\n", sizeof(ttt_config));
   F(ttt_config, n_layers) F(ttt_config, window) F(ttt_config, n_seqs) F(ttt_config, rope_theta)
-  F(ttt_config, rms_eps) F(ttt_config, eta) F(ttt_config, compute)
+  F(ttt_config, rms_eps) F(ttt_config, eta) F(ttt_config, compute) F(ttt_config, dual_mlp)
   printf("ttt_kernel_stat %zu\n", sizeof(ttt_kernel_stat));
   F(ttt_kernel_stat, launches) F(ttt_kernel_stat, ms) F(ttt_kernel_stat, bytes)
   printf("ttt_gemm_epilogue %zu\n", sizeof(ttt_gemm_epilogue));
@@ -96,6 +96,7 @@ def _create(cfg):
     dict(d_model=130, n_heads=4),         # d not divisible by H
     dict(n_seqs=0),
     dict(compute=2),
+    dict(dual_mlp=2),
 ])
 def test_create_rejects_inconsistent_configs_before_any_cuda_call(bad):
     cfg = T.make_config(4, 128, 4, 512, 512, 128, 64, 1e4, 1e-2)
@@ -139,6 +140,7 @@ def test_kernel_entry_points_reject_bad_arguments():
 def test_context_calls_reject_null_context():
     assert T.ttt_load_weights(None, 1, 10) == T.TTT_ERR_ARG
     assert T.ttt_prefill_chunk(None, 1, 1, 1, 1) == T.TTT_ERR_ARG
+    assert T.ttt_prefill_sequence(None, 1, 1, 1) == T.TTT_ERR_ARG
     assert T.ttt_get_fast_weights(None, 0, 0, None, None) == T.TTT_ERR_ARG
     assert T.ttt_reset(None) == T.TTT_ERR_ARG
     assert T.ttt_launch_count(None) == -1

@@ -49,6 +49,12 @@ CASES = [  # n, H, dh, window, pos0, split
     (37, 2, 64, 256, 700, False),
     (512, 2, 96, 1024, 1500, False),   # two 256-query blocks, cache wraps, unaligned start
     (384, 2, 64, 512, 640, False),     # second block half full
+    # the benchmark's geometry: a trainable-block step (1024 queries, 72 key tiles per query
+    # tile, full 8192-slot cache) at head widths 96 (760M) and 128 (3B), and a frozen-block
+    # pass (8192 queries starting at a multiple of the window)
+    (1024, 2, 96, 8192, 20000, False),
+    (1024, 1, 128, 8192, 20000, False),
+    (8192, 1, 96, 8192, 16384, False),
 ]
 
 

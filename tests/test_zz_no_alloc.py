@@ -6,8 +6,10 @@ cudaMalloc's implicit device synchronisation.  For them the library keeps this
 variant's scratch in a static device array.  This test checks, through the C
 ABI, that two calls in a row give the same per-row log-sum-exp and loss as the
 allocating path (ttt_k_gemm with the CE_FWD epilogue into caller scratch, its
-partials combined here in float64), within the tolerance of the GEMM tests,
-and that a size beyond the static capacity is refused.
+partials combined here in float64) and as a float64 numpy computation from the
+same bf16 inputs, within the tolerance of the GEMM tests; that the second call
+leaves the device's free memory unchanged; and that a size beyond the static
+capacity is refused.
 
 The file sorts last so that a run stopping at the first failure has already
 run every other test; it passes alone in a fresh process as well.
@@ -30,18 +32,22 @@ def rel(x, y):
 
 
 def reference_from_allocating_path(M, K, V, x, w, tgt):
-    """lse / loss from ttt_k_gemm(CE_FWD) with caller-allocated partials."""
-    ntiles = -(-V // 128)                          # enough for either tile width
-    part = torch.zeros(ntiles * M * 2, dtype=torch.float32, device=dev)
+    """lse / loss from ttt_k_gemm(CE_FWD) with caller-allocated partials.
+
+    The partials are laid out [vocab tile][row]; every pair starts as (-inf, 0),
+    so combining over the 128-wide tile count is right whichever tile width
+    the library picks (tiles it does not write add exp(-inf) * 0 = 0).
+    """
+    ntiles = -(-V // 128)
+    part = torch.zeros((ntiles * M, 2), dtype=torch.float32, device=dev)
+    part[:, 0] = float("-inf")
     zt = torch.zeros(M, dtype=torch.float32, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     T.gemm(T.EPI_CE_FWD, M, V, K, x, w, b_mn=1, tgt=tgt, part=part, zt=zt, err=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
-    p = part.cpu().numpy().astype(np.float64).reshape(-1, 2)
+    pm = part.cpu().numpy().astype(np.float64).reshape(ntiles, M, 2)
     t = tgt.cpu().numpy()
-    nt = -(-V // _tile_width(M, V))
-    pm = p[:nt * M].reshape(nt, M, 2)
     mx = pm[:, :, 0].max(0)
     lse = mx + np.log((pm[:, :, 1] * np.exp(pm[:, :, 0] - mx)).sum(0))
     z_t = zt.cpu().numpy().astype(np.float64)
@@ -49,13 +55,14 @@ def reference_from_allocating_path(M, K, V, x, w, tgt):
     return lse, loss
 
 
-def _tile_width(M, V):
-    """The vocab tile width the library picks for an M x V product (fewest tile-columns per SM)."""
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    mt = -(-M // 128)
-    t256, t128 = mt * -(-V // 256), mt * -(-V // 128)
-    c256, c128 = -(-t256 // sms) * 256, -(-t128 // sms) * 128
-    return 128 if (V <= 128 or c128 < c256) else 256
+def reference_float64(x, w, tgt):
+    """lse = logsumexp(x . W) and loss = lse - z[tgt], in numpy float64 from the bf16 inputs."""
+    z = x.double().cpu().numpy() @ w.double().cpu().numpy()
+    m = z.max(1)
+    lse = m + np.log(np.exp(z - m[:, None]).sum(1))
+    t = tgt.cpu().numpy()
+    loss = np.where(t >= 0, lse - z[np.arange(len(t)), np.maximum(t, 0)], 0.0)
+    return lse, loss
 
 
 @pytest.mark.parametrize("M,K,V", [(300, 128, 1000), (1024, 768, 32000)])
@@ -67,18 +74,25 @@ def test_static_scratch_matches_allocating_path_twice(M, K, V):
     t[::7] = -1
     tgt = torch.tensor(t, device=dev)
     lse_ref, loss_ref = reference_from_allocating_path(M, K, V, x, w, tgt)
+    lse64, loss64 = reference_float64(x, w, tgt)
+    assert rel(lse_ref, lse64) < 1e-5 and rel(loss_ref, loss64) < 1e-5
     for call in range(2):
+        free0, _ = torch.cuda.mem_get_info()
         lse = torch.full((M,), float("nan"), dtype=torch.float32, device=dev)
         loss = torch.full((M,), float("nan"), dtype=torch.float32, device=dev)
         err = torch.zeros(1, dtype=torch.int32, device=dev)
         T.lmhead_ce_static(M, K, V, x, w, tgt, lse, loss, err=err)
         torch.cuda.synchronize()
+        free1, _ = torch.cuda.mem_get_info()
+        if call == 1:  # the array is in place after the first call: nothing is allocated any more
+            assert free1 == free0, (free0, free1)
         assert int(err.item()) == 0
         got_lse = lse.cpu().numpy().astype(np.float64)
         got_loss = loss.cpu().numpy().astype(np.float64)
         assert np.all(np.isfinite(got_lse)) and np.all(np.isfinite(got_loss)), call
         assert rel(got_lse, lse_ref) < 1e-5, call
         assert rel(got_loss, loss_ref) < 1e-5, call
+        assert rel(got_lse, lse64) < 1e-5 and rel(got_loss, loss64) < 1e-5, call
         assert np.all(got_loss[t < 0] == 0.0), call
 
 
