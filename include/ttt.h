@@ -140,6 +140,35 @@ TTT_API int ttt_prefill_sequence_dev(ttt_ctx* ctx, const int32_t* d_tokens, int3
  */
 TTT_API int ttt_prefill_sequence(ttt_ctx* ctx, const int32_t* tokens, int32_t T, float* losses);
 
+/*
+ * Decode-phase TTT with DEVICE buffers (pages: "TTT-E2E技术：突破大语言模型上下文限制的新范式",
+ * §2.2 "批量更新与稳定性控制": one update per chunk of input tokens while prefilling and
+ * one per chunk of generated tokens while generating; "把 Transformer 做成“终身学习者”",
+ * §4.2: the inner loop is reused at inference).  For every sequence:
+ *   1. the prompt (d_prompt int32 [n_seqs][T]) goes through the chunked inner loop
+ *      as in ttt_prefill_sequence_dev (its last position has no target);
+ *      chunk losses -> d_prefill_losses float [n_seqs][ceil(T/b)];
+ *   2. the token at position t is picked from the logits of position t - 1, as the
+ *      forward of t - 1's chunk computes them, before that chunk's update; the first
+ *      one comes from the prompt's last position.  sample = 0: the first index of
+ *      the largest logit; sample = 1: inverse CDF of softmax(z / temp) at the caller's
+ *      uniform u[i] (d_u float [n_seqs][n_new + 1], in [0, 1)) -- the first index
+ *      whose running sum of exp(z/temp - max) exceeds u[i] times the total;
+ *   3. generated tokens form chunks of b from the first generated position; each
+ *      complete chunk takes one inner-loop step (forward, mean next-token loss whose
+ *      last target is the token picked after the chunk, suffix backward, SGD, cache
+ *      commit) -> d_gen_losses float [n_seqs][n_new / b] (may be NULL if n_new < b);
+ *      an incomplete last chunk takes no step.
+ * d_out int32 [n_seqs][n_new + 1]: the n_new generated ids, then the id picked after
+ * them.  d_logits (optional) float [n_seqs][n_new + 1][V]: the logits row behind each
+ * pick.  Every generated token is one forward over one row per block (bf16 or split
+ * products as in prefill); ids never leave the device.  Asynchronous like the other
+ * _dev calls; sequences continue from their current position and fast weights.
+ */
+TTT_API int ttt_decode_dev(ttt_ctx* ctx, const int32_t* d_prompt, int32_t T, int32_t n_new, int32_t sample,
+                           float temp, const float* d_u, int32_t* d_out, float* d_prefill_losses,
+                           float* d_gen_losses, float* d_logits);
+
 /* Wait for the context stream and report a device-side error (TTT_ERR_DEVICE). */
 TTT_API int ttt_sync(ttt_ctx* ctx);
 
@@ -159,6 +188,30 @@ TTT_API int ttt_get_fast_weights(ttt_ctx* ctx, int32_t seq, int32_t suffix_layer
  * Any output may be NULL.  Synchronises the context stream.
  */
 TTT_API int ttt_get_window(ttt_ctx* ctx, int32_t seq, int32_t layer, float* k_out, float* v_out, int64_t* pos_out);
+
+/*
+ * Resumable state of one sequence (pages: "TTT-E2E技术：突破大语言模型上下文限制的新范式",
+ * §5.1, the adapted "personal parameters" kept per user; "把 Transformer 做成“终身学习者”",
+ * §4.2, the window cache the next chunk reads): its position, its fp32 fast
+ * weights and its key/value window cache, as one host byte buffer.
+ *   ttt_state_bytes   size of that buffer for this context's shape (-1 for NULL)
+ *   ttt_export_state  synchronises the context stream, then copies sequence
+ *                     `seq`'s state into host_buf (exactly ttt_state_bytes bytes)
+ *   ttt_import_state  replaces sequence `seq`'s state by an exported one; the
+ *                     context must be loaded and of the same shape (layers,
+ *                     trainable blocks, widths, window, compute mode, dual-MLP),
+ *                     else TTT_ERR_ARG; the fast weights' bf16 shadows are derived
+ *                     again on the device.  Synchronises.
+ * Layout: a 48-byte header ("TTTSTAT1", L, S, d, d_ff, window, fp32 mode,
+ * dual-MLP, pad, int64 position), W_up fp32 [S][d][d_ff], W_down fp32
+ * [S][d_ff][d], then the cache keys and values bf16 [L][window][d] (then
+ * their bf16 remainders in the fp32 mode), slot = position mod window.
+ * Exporting after chunk i and importing into a fresh context continues the
+ * sequence from chunk i + 1 with the same results.
+ */
+TTT_API int64_t ttt_state_bytes(const ttt_ctx* ctx);
+TTT_API int ttt_export_state(ttt_ctx* ctx, int32_t seq, void* host_buf, size_t bytes);
+TTT_API int ttt_import_state(ttt_ctx* ctx, int32_t seq, const void* host_buf, size_t bytes);
 
 /*
  * Restart every sequence from the loaded weights without re-uploading them:

@@ -123,6 +123,7 @@ ttt_prefill_chunk = _sig("ttt_prefill_chunk", ctypes.c_int, _vp, _vp, _i32, _vp,
 ttt_prefill_chunk_dev = _sig("ttt_prefill_chunk_dev", ctypes.c_int, _vp, _vp, _i32, _vp, _vp)
 ttt_prefill_sequence_dev = _sig("ttt_prefill_sequence_dev", ctypes.c_int, _vp, _vp, _i32, _vp)
 ttt_prefill_sequence = _sig("ttt_prefill_sequence", ctypes.c_int, _vp, _vp, _i32, _vp)
+ttt_decode_dev = _sig("ttt_decode_dev", ctypes.c_int, _vp, _vp, _i32, _i32, _i32, _f32, _vp, _vp, _vp, _vp, _vp)
 ttt_sync = _sig("ttt_sync", ctypes.c_int, _vp)
 ttt_get_fast_weights = _sig("ttt_get_fast_weights", ctypes.c_int, _vp, _i32, _i32, _vp, _vp)
 ttt_position = _sig("ttt_position", _i64, _vp)
@@ -131,6 +132,9 @@ ttt_last_error = _sig("ttt_last_error", ctypes.c_char_p, _vp)
 ttt_reset = _sig("ttt_reset", ctypes.c_int, _vp)
 ttt_get_window = _sig("ttt_get_window", ctypes.c_int, _vp, _i32, _i32, _vp, _vp, _vp)
 ttt_launch_count = _sig("ttt_launch_count", _i64, _vp)
+ttt_state_bytes = _sig("ttt_state_bytes", _i64, _vp)
+ttt_export_state = _sig("ttt_export_state", ctypes.c_int, _vp, _i32, _vp, ctypes.c_size_t)
+ttt_import_state = _sig("ttt_import_state", ctypes.c_int, _vp, _i32, _vp, ctypes.c_size_t)
 
 
 class ttt_kernel_stat(ctypes.Structure):
@@ -258,6 +262,13 @@ class TTT:
                     "ttt_prefill_sequence")
         return losses
 
+    def decode_dev(self, d_prompt, T, n_new, d_out, d_prefill_losses, d_gen_losses=None, *, sample=False,
+                   temp=1.0, d_u=None, d_logits=None):
+        """ttt_decode_dev on device tensors (see include/ttt.h)."""
+        self._check(ttt_decode_dev(self._h, ptr(d_prompt), T, n_new, int(sample), float(temp), ptr(d_u),
+                                   ptr(d_out), ptr(d_prefill_losses), ptr(d_gen_losses), ptr(d_logits)),
+                    "ttt_decode_dev")
+
     def sync(self):
         self._check(ttt_sync(self._h), "ttt_sync")
 
@@ -278,6 +289,16 @@ class TTT:
         self._check(ttt_get_window(self._h, seq, layer, ko.ctypes.data, vo.ctypes.data, po.ctypes.data),
                     "ttt_get_window")
         return ko, vo, po
+
+    def export_state(self, seq: int = 0) -> bytes:
+        """Position, fast weights and window cache of one sequence as bytes (ttt_export_state)."""
+        buf = np.zeros(int(ttt_state_bytes(self._h)), np.uint8)
+        self._check(ttt_export_state(self._h, seq, buf.ctypes.data, buf.size), "ttt_export_state")
+        return buf.tobytes()
+
+    def import_state(self, state: bytes, seq: int = 0):
+        buf = np.frombuffer(state, np.uint8)
+        self._check(ttt_import_state(self._h, seq, buf.ctypes.data, buf.size), "ttt_import_state")
 
     def reset(self):
         self._check(ttt_reset(self._h), "ttt_reset")

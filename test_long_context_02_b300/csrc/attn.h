@@ -16,6 +16,7 @@ struct AttnArgs {
   bf16* o_hi = nullptr; bf16* o_lo = nullptr; long ldo = 0;   // forward output [n][d]
   float* lse = nullptr; // [H][n] log2-sum-exp of the scaled scores (optional)
   int* err = nullptr;
+  int qt0 = 0;          // forward only: first query tile computed (earlier rows are left as they are)
 };
 
 // TMA maps (box {64, 128}) of: queries [n][d]; cache keys/values [k][d];
@@ -46,11 +47,10 @@ struct AttnBwdMaps {
   CUtensorMap dO, dOl; // output gradient [n][d]
 };
 
-// which: 0 = both kernels, 1 = dQ only, 2 = dK/dV only
+// dQ (dS kept in TMEM, attn_dq2.cuh) and dK/dV (P^T, dS^T kept in TMEM,
+// attn_dkv2.cuh) in one launch (attn_bwd.cu); which: 0 = both, 1 = dQ only,
+// 2 = dK/dV only.
 int attn_bwd_run(const AttnBwdMaps& m, const AttnBwdArgs& a, bool split, cudaStream_t st, int which = 0);
-// dQ with dS kept in TMEM (attn_dq2.cu); dK/dV with P^T, dS^T kept in TMEM (attn_dkv2.cu).
-int attn_dq2_run(const AttnBwdMaps& m, const AttnBwdArgs& a, bool split, cudaStream_t st);
-int attn_dkv2_run(const AttnBwdMaps& m, const AttnBwdArgs& a, bool split, cudaStream_t st);
 
 
 }  // namespace ttt

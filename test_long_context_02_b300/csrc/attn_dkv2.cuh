@@ -17,6 +17,7 @@
 // Warps 2-9 (two threads per key row, 64 query columns each) form P^T from S^T
 // and the stored statistics, write it as bf16 over their own S^T columns, then
 // dS^T over their own dP^T columns.
+#pragma once
 #include "attn.h"
 #include "kernels.h"
 #include "ptx.cuh"
@@ -92,13 +93,11 @@ TTT_DEV void pack64(const float* x, uint32_t (&hi)[32], uint32_t (&lo)[32]) {
   }
 }
 
+// One CTA of dK / dV: own-key tile kt of head h.
 template <int DH, bool SPLIT>
-__global__ void __launch_bounds__(kK2Threads, 1)
-    attn_dkv2_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap tQl,
-                     const __grid_constant__ CUtensorMap tDO, const __grid_constant__ CUtensorMap tDOl,
-                     const __grid_constant__ CUtensorMap tKo, const __grid_constant__ CUtensorMap tKol,
-                     const __grid_constant__ CUtensorMap tVo, const __grid_constant__ CUtensorMap tVol,
-                     const AttnBwdArgs a) {
+TTT_DEV void dkv2_body(const CUtensorMap* tQ, const CUtensorMap* tQl, const CUtensorMap* tDO, const CUtensorMap* tDOl,
+                       const CUtensorMap* tKo, const CUtensorMap* tKol, const CUtensorMap* tVo, const CUtensorMap* tVol,
+                       const AttnBwdArgs& a, const int kt, const int h) {
   using C = K2Cfg<DH, SPLIT>;
   constexpr int HO = DH / 2;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -122,7 +121,6 @@ __global__ void __launch_bounds__(kK2Threads, 1)
 
   const AttnArgs& g = a.g;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int kt = blockIdx.x, h = blockIdx.y;
   const int nq = (g.n + 127) / 128;
   const int I = nq - kt;  // causal query tiles kt .. nq-1
   const int col0 = h * DH;
@@ -156,11 +154,11 @@ __global__ void __launch_bounds__(kK2Threads, 1)
     uint32_t iss = 0, ipar = 0;
     if (lane == 0) {
       mbar_expect_tx(kv_full, 2 * C::NOP * C::TILE);
-      load_tile_k2<C::NATOM>(smem + C::K_OFF, &tKo, kv_full, col0, 128 * kt);
-      load_tile_k2<C::NATOM>(smem + C::V_OFF, &tVo, kv_full, col0, 128 * kt);
+      load_tile_k2<C::NATOM>(smem + C::K_OFF, tKo, kv_full, col0, 128 * kt);
+      load_tile_k2<C::NATOM>(smem + C::V_OFF, tVo, kv_full, col0, 128 * kt);
       if (SPLIT) {
-        load_tile_k2<C::NATOM>(smem + C::K_OFF + C::TILE, &tKol, kv_full, col0, 128 * kt);
-        load_tile_k2<C::NATOM>(smem + C::V_OFF + C::TILE, &tVol, kv_full, col0, 128 * kt);
+        load_tile_k2<C::NATOM>(smem + C::K_OFF + C::TILE, tKol, kv_full, col0, 128 * kt);
+        load_tile_k2<C::NATOM>(smem + C::V_OFF + C::TILE, tVol, kv_full, col0, 128 * kt);
       }
     }
     for (int i = 0; i < I; ++i) {
@@ -172,11 +170,11 @@ __global__ void __launch_bounds__(kK2Threads, 1)
       if (lane == 0) {
         uint8_t* st = smem + C::Q_OFF + s * C::STAGE;
         mbar_expect_tx(&qd_full[s], 2 * C::NOP * C::TILE);
-        load_tile_k2<C::NATOM>(st, &tQ, &qd_full[s], col0, q0);
-        load_tile_k2<C::NATOM>(st + C::NOP * C::TILE, &tDO, &qd_full[s], col0, q0);
+        load_tile_k2<C::NATOM>(st, tQ, &qd_full[s], col0, q0);
+        load_tile_k2<C::NATOM>(st + C::NOP * C::TILE, tDO, &qd_full[s], col0, q0);
         if (SPLIT) {
-          load_tile_k2<C::NATOM>(st + C::TILE, &tQl, &qd_full[s], col0, q0);
-          load_tile_k2<C::NATOM>(st + C::NOP * C::TILE + C::TILE, &tDOl, &qd_full[s], col0, q0);
+          load_tile_k2<C::NATOM>(st + C::TILE, tQl, &qd_full[s], col0, q0);
+          load_tile_k2<C::NATOM>(st + C::NOP * C::TILE + C::TILE, tDOl, &qd_full[s], col0, q0);
         }
         iss |= 1u << s;
         ipar = (ipar & ~(1u << s)) | (par << s);
@@ -330,39 +328,6 @@ __global__ void __launch_bounds__(kK2Threads, 1)
   }
 }
 
-template <int DH, bool SPLIT>
-int launch_dkv2(const AttnBwdMaps& m, const AttnBwdArgs& a, cudaStream_t st) {
-  using C = K2Cfg<DH, SPLIT>;
-  auto kern = attn_dkv2_kernel<DH, SPLIT>;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return (int)e;
-    attr = true;
-  }
-  dim3 grid((a.g.n + 127) / 128, a.g.H);
-  const AttnMaps& f = m.f;
-  return (int)launch_k(kern, grid, dim3(kK2Threads), C::SMEM, st, f.q, f.ql, m.dO, m.dOl, f.ko, f.kol, f.vo, f.vol, a);
-}
-
 }  // namespace
-
-int attn_dkv2_run(const AttnBwdMaps& m, const AttnBwdArgs& a, bool split, cudaStream_t st) {
-  if (a.g.n <= 0) return 0;
-  if (split) {
-    switch (a.g.dh) {
-      case 32: return launch_dkv2<32, true>(m, a, st);
-      case 64: return launch_dkv2<64, true>(m, a, st);
-    }
-    return (int)cudaErrorInvalidValue;
-  }
-  switch (a.g.dh) {
-    case 32: return launch_dkv2<32, false>(m, a, st);
-    case 64: return launch_dkv2<64, false>(m, a, st);
-    case 96: return launch_dkv2<96, false>(m, a, st);
-    case 128: return launch_dkv2<128, false>(m, a, st);
-  }
-  return (int)cudaErrorInvalidValue;
-}
 
 }  // namespace ttt

@@ -13,6 +13,7 @@
 // TMEM.  Warps 2-9 (two threads per query row, 64 key columns each) form dS_j
 // from S_j, dP_j and the row statistics and write it as bf16 over their own
 // columns of S_j.
+#pragma once
 #include "attn.h"
 #include "kernels.h"
 #include "ptx.cuh"
@@ -92,15 +93,13 @@ TTT_DEV RangeQ2 range_q2(const AttnArgs& a, int qt) {
   return r;
 }
 
+// One CTA of dQ: query tile qt of head h.  The tensor maps are the kernel's
+// __grid_constant__ parameters.
 template <int DH, bool SPLIT>
-__global__ void __launch_bounds__(kQ2Threads, 1)
-    attn_dq2_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap tQl,
-                    const __grid_constant__ CUtensorMap tDO, const __grid_constant__ CUtensorMap tDOl,
-                    const __grid_constant__ CUtensorMap tKr, const __grid_constant__ CUtensorMap tKrl,
-                    const __grid_constant__ CUtensorMap tVr, const __grid_constant__ CUtensorMap tVrl,
-                    const __grid_constant__ CUtensorMap tKo, const __grid_constant__ CUtensorMap tKol,
-                    const __grid_constant__ CUtensorMap tVo, const __grid_constant__ CUtensorMap tVol,
-                    const AttnBwdArgs a) {
+TTT_DEV void dq2_body(const CUtensorMap* tQ, const CUtensorMap* tQl, const CUtensorMap* tDO, const CUtensorMap* tDOl,
+                      const CUtensorMap* tKr, const CUtensorMap* tKrl, const CUtensorMap* tVr, const CUtensorMap* tVrl,
+                      const CUtensorMap* tKo, const CUtensorMap* tKol, const CUtensorMap* tVo, const CUtensorMap* tVol,
+                      const AttnBwdArgs& a, const int qt, const int h) {
   using C = Q2Cfg<DH, SPLIT>;
   constexpr int HO = DH / 2;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -123,7 +122,6 @@ __global__ void __launch_bounds__(kQ2Threads, 1)
 
   const AttnArgs& g = a.g;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qt = blockIdx.x, h = blockIdx.y;
   const RangeQ2 tr = range_q2(g, qt);
   const int J = tr.J;
   const int col0 = h * DH;
@@ -166,11 +164,11 @@ __global__ void __launch_bounds__(kQ2Threads, 1)
     if (lane == 0) {  // ---------------------------------------------------- TMA producer
       uint32_t kiss = 0, kpar = 0, viss = 0, vpar = 0;
       mbar_expect_tx(q_full, 2 * C::NOP * C::TILE);
-      load_tile_q2<C::NATOM>(smem + C::Q_OFF, &tQ, q_full, col0, 128 * qt);
-      load_tile_q2<C::NATOM>(smem + C::DO_OFF, &tDO, q_full, col0, 128 * qt);
+      load_tile_q2<C::NATOM>(smem + C::Q_OFF, tQ, q_full, col0, 128 * qt);
+      load_tile_q2<C::NATOM>(smem + C::DO_OFF, tDO, q_full, col0, 128 * qt);
       if (SPLIT) {
-        load_tile_q2<C::NATOM>(smem + C::Q_OFF + C::TILE, &tQl, q_full, col0, 128 * qt);
-        load_tile_q2<C::NATOM>(smem + C::DO_OFF + C::TILE, &tDOl, q_full, col0, 128 * qt);
+        load_tile_q2<C::NATOM>(smem + C::Q_OFF + C::TILE, tQl, q_full, col0, 128 * qt);
+        load_tile_q2<C::NATOM>(smem + C::DO_OFF + C::TILE, tDOl, q_full, col0, 128 * qt);
       }
       for (int j = 0; j < J; ++j) {
         const int s = j & 1;
@@ -180,15 +178,15 @@ __global__ void __launch_bounds__(kQ2Threads, 1)
         if (!mbar_wait(&k_empty[s], par ^ 1u, abort_flag, g.err, DERR_TIMEOUT_PRODUCER)) break;
         uint8_t* kd = smem + C::K_OFF + s * C::NOP * C::TILE;
         mbar_expect_tx(&k_full[s], C::NOP * C::TILE);
-        load_tile_q2<C::NATOM>(kd, own ? &tKo : &tKr, &k_full[s], col0, row0);
-        if (SPLIT) load_tile_q2<C::NATOM>(kd + C::TILE, own ? &tKol : &tKrl, &k_full[s], col0, row0);
+        load_tile_q2<C::NATOM>(kd, own ? tKo : tKr, &k_full[s], col0, row0);
+        if (SPLIT) load_tile_q2<C::NATOM>(kd + C::TILE, own ? tKol : tKrl, &k_full[s], col0, row0);
         kiss |= 1u << s;
         kpar = (kpar & ~(1u << s)) | (par << s);
         if (!mbar_wait(&v_empty[s], par ^ 1u, abort_flag, g.err, DERR_TIMEOUT_PRODUCER)) break;
         uint8_t* vd = smem + C::V_OFF + s * C::NOP * C::TILE;
         mbar_expect_tx(&v_full[s], C::NOP * C::TILE);
-        load_tile_q2<C::NATOM>(vd, own ? &tVo : &tVr, &v_full[s], col0, row0);
-        if (SPLIT) load_tile_q2<C::NATOM>(vd + C::TILE, own ? &tVol : &tVrl, &v_full[s], col0, row0);
+        load_tile_q2<C::NATOM>(vd, own ? tVo : tVr, &v_full[s], col0, row0);
+        if (SPLIT) load_tile_q2<C::NATOM>(vd + C::TILE, own ? tVol : tVrl, &v_full[s], col0, row0);
         viss |= 1u << s;
         vpar = (vpar & ~(1u << s)) | (par << s);
       }
@@ -329,40 +327,6 @@ __global__ void __launch_bounds__(kQ2Threads, 1)
   }
 }
 
-template <int DH, bool SPLIT>
-int launch_dq2(const AttnBwdMaps& m, const AttnBwdArgs& a, cudaStream_t st) {
-  using C = Q2Cfg<DH, SPLIT>;
-  auto kern = attn_dq2_kernel<DH, SPLIT>;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return (int)e;
-    attr = true;
-  }
-  dim3 grid((a.g.n + 127) / 128, a.g.H);
-  const AttnMaps& f = m.f;
-  return (int)launch_k(kern, grid, dim3(kQ2Threads), C::SMEM, st, f.q, f.ql, m.dO, m.dOl, f.kr, f.krl, f.vr, f.vrl,
-                       f.ko, f.kol, f.vo, f.vol, a);
-}
-
 }  // namespace
-
-int attn_dq2_run(const AttnBwdMaps& m, const AttnBwdArgs& a, bool split, cudaStream_t st) {
-  if (a.g.n <= 0) return 0;
-  if (split) {
-    switch (a.g.dh) {
-      case 32: return launch_dq2<32, true>(m, a, st);
-      case 64: return launch_dq2<64, true>(m, a, st);
-    }
-    return (int)cudaErrorInvalidValue;
-  }
-  switch (a.g.dh) {
-    case 32: return launch_dq2<32, false>(m, a, st);
-    case 64: return launch_dq2<64, false>(m, a, st);
-    case 96: return launch_dq2<96, false>(m, a, st);
-    case 128: return launch_dq2<128, false>(m, a, st);
-  }
-  return (int)cudaErrorInvalidValue;
-}
 
 }  // namespace ttt

@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(kF3Threads, 1)
   float* xch = reinterpret_cast<float*>(smem + C::XCH_OFF);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qt = blockIdx.x, h = blockIdx.y;
+  const int qt = (int)blockIdx.x + a.qt0, h = blockIdx.y;
   const Range3 tr = range3(a, qt);
   const int J = tr.J;
   const int col0 = h * DH;
@@ -434,7 +434,7 @@ int launch_fwd3(const AttnMaps& m, const AttnArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return (int)e;
     attr = true;
   }
-  dim3 grid((a.n + 127) / 128, a.H);
+  dim3 grid((a.n + 127) / 128 - a.qt0, a.H);
   return (int)launch_k(kern, grid, dim3(kF3Threads), C::SMEM, st, m.q, m.ql, m.kr, m.krl, m.vr, m.vrl, m.ko, m.kol,
                        m.vo, m.vol, a);
 }

@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(kF5Threads, 1)
   float* xch = reinterpret_cast<float*>(smem + C::XCH_OFF);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qt = blockIdx.x, h = blockIdx.y;
+  const int qt = (int)blockIdx.x + a.qt0, h = blockIdx.y;
   const Range5 tr = range5(a, qt);
   const int J = tr.J;
   const int col0 = h * DH;
@@ -404,7 +404,7 @@ int launch_fwd5(const AttnMaps& m, const AttnArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return (int)e;
     attr = true;
   }
-  dim3 grid((a.n + 127) / 128, a.H);
+  dim3 grid((a.n + 127) / 128 - a.qt0, a.H);
   return (int)launch_k(kern, grid, dim3(kF5Threads), C::SMEM, st, m.q, m.kr, m.vr, m.ko, m.vo, a);
 }
 

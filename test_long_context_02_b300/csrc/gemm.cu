@@ -251,10 +251,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       bool ok = true;
       uint32_t issued = 0;  // bit s: stage s has a fill in flight or landed
       uint32_t iss_par = 0; // bit s: parity of that fill
+      // fp32 operand the epilogue reads (residual, GELU argument, fp32 weights): its tile is
+      // brought into L2 while the tile's mainloop runs, so the epilogue does not wait on HBM
+      constexpr bool kEpiIn = EPI == EPI_RESID || EPI == EPI_GELU_BWD || EPI == EPI_SGD;
+      const float* ein = EPI == EPI_RESID ? g.resid : (EPI == EPI_GELU_BWD ? g.aux : g.w32);
+      const long ldein = EPI == EPI_RESID ? g.ldr : (EPI == EPI_GELU_BWD ? g.ldaux : g.ldw);
+      const bool pf = kEpiIn && ein != nullptr && !(EPI == EPI_RESID && ks > 1) && (ldein & 3) == 0;
       for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
         const int t = u % ntiles, sl = u / ntiles;
         const int m0 = (t % mt) * BM, n0 = (t / mt) * BN;
         const int kb0 = (int)((long)sl * nk / ks), kb1 = (int)((long)(sl + 1) * nk / ks);
+        if (pf) {
+          const uint32_t bytes = (uint32_t)(min(BN, g.N - n0) * 4) & ~15u;
+          const int r1 = min(m0 + BM, g.M);
+          for (int r = m0; r < r1 && bytes; ++r) {
+            const float* a = ein + (long)r * ldein + n0;
+            if ((reinterpret_cast<uintptr_t>(a) & 15u) == 0) prefetch_l2(a, bytes);
+          }
+        }
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, g.err, DERR_TIMEOUT_PRODUCER)) {
             ok = false;
@@ -634,14 +648,26 @@ int dispatch_epi(int epi, const CUtensorMap& a, const CUtensorMap& al, const CUt
 
 // Tile width for N: the one that needs the fewest tile-columns of work per SM
 // (waves x BN), preferring the wider tile on a tie.
+// Weight of a tile width in the cost model: its MMA rate per byte of shared memory
+// against the 256-wide tile (measured ~0.6 for 128 wide; 192 wide reads 11 % more
+// operand bytes per product).
+double bn_weight(int bn) { return bn == 256 ? 1.0 : (bn == 192 ? 1.1 : 1.6); }
+
 int pick_bn(int M, int N) {
   const int sms = num_sms();
-  const int mt = (M + BM - 1) / BM;
-  const long t256 = (long)mt * ((N + 255) / 256), t128 = (long)mt * ((N + 127) / 128);
-  // waves x tile width, the 128-wide tile weighted by its lower MMA rate per byte of
-  // shared memory (measured ~0.6 of the 256-wide tile on the same product)
-  const double c256 = (double)((t256 + sms - 1) / sms) * 256, c128 = (double)((t128 + sms - 1) / sms) * 128 * 1.6;
-  return (N <= 128 || c128 < c256) ? 128 : 256;
+  const long mt = (M + BM - 1) / BM;
+  if (N <= 128) return 128;
+  int best = 256;
+  double bc = -1;
+  for (int bn : {256, 192, 128}) {  // waves x tile width x weight; the wider tile on a tie
+    const long t = mt * ((N + bn - 1) / bn);
+    const double c = (double)((t + sms - 1) / sms) * bn * bn_weight(bn);
+    if (bc < 0 || c < bc) {
+      bc = c;
+      best = bn;
+    }
+  }
+  return best;
 }
 
 // Tile width of the fused QKV + RoPE product for head width dh and model width d
@@ -699,15 +725,15 @@ void choose_tiling(int M, int N, int K, bool allow_slices, int* bn_out, int* ks_
   const long sms = num_sms();
   const long mt = (M + BM - 1) / BM, nk = (K + BK - 1) / BK;
   double best = -1;
-  for (int bn : {256, 128}) {
-    if (bn == 256 && N <= 128) continue;
+  for (int bn : {256, 192, 128}) {
+    if (bn > 128 && N <= 128) continue;
     const long tiles = mt * ((N + bn - 1) / bn);
     for (int ks = 1; ks <= (allow_slices ? 8 : 1); ++ks) {
       if (ks > 1 && nk / ks < 4) break;
       const long units = tiles * ks;
       // per unit: its k-blocks, plus about two k-blocks' worth for the atomic epilogue of a slice;
-      // the 128-wide tile weighted as in pick_bn
-      const double cost = (double)((units + sms - 1) / sms) * bn * (bn == 128 ? 1.6 : 1.0) *
+      // tile widths weighted as in pick_bn
+      const double cost = (double)((units + sms - 1) / sms) * bn * bn_weight(bn) *
                           ((nk + ks - 1) / ks + (ks > 1 ? 2 : 0));
       if (best < 0 || cost < best) {
         best = cost;
@@ -747,6 +773,8 @@ int gemm_run(int epi, const Opnd& A, const Opnd& B, GemmArgs g, bool split, cuda
     return (int)cudaErrorInvalidValue;
   if (bn == 128)
     return split ? dispatch_epi<128, true>(epi, a, al, b, bl, g, st) : dispatch_epi<128, false>(epi, a, al, b, bl, g, st);
+  if (bn == 192)
+    return split ? dispatch_epi<192, true>(epi, a, al, b, bl, g, st) : dispatch_epi<192, false>(epi, a, al, b, bl, g, st);
   return split ? dispatch_epi<256, true>(epi, a, al, b, bl, g, st) : dispatch_epi<256, false>(epi, a, al, b, bl, g, st);
 }
 

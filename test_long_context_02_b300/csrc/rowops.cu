@@ -395,7 +395,98 @@ __global__ void convert_kernel(const float* __restrict__ src, long rows, int col
 constexpr int kRowWarps = 8;
 inline int row_grid(int n) { return (n + kRowWarps - 1) / kRowWarps; }
 
+// Next token from one row of logits z[V] (decode-phase TTT).  Greedy: the first
+// index of the largest logit.  Sampling: inverse CDF of softmax(z / temp) at the
+// caller's uniform *u: the first index whose running sum of exp(z/temp - max)
+// exceeds *u times the total.  One block; thread t owns the contiguous run
+// [t*per, (t+1)*per) of the vocabulary, so running sums follow index order.
+constexpr int kPickThreads = 1024;
+__global__ void __launch_bounds__(kPickThreads)
+    pick_kernel(const float* __restrict__ z, int V, int sample, float temp, const float* __restrict__ u,
+                int* __restrict__ out) {
+  pdl_wait();
+  pdl_launch_dependents();
+  __shared__ float s_v[32];
+  __shared__ int s_i[32];
+  __shared__ float s_sum[32];
+  __shared__ int s_pick;
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const int per = (V + kPickThreads - 1) / kPickThreads;
+  const int j0 = min(V, t * per), j1 = min(V, j0 + per);
+  auto val = [&](int j) { return sample ? z[j] / temp : z[j]; };
+  // largest value, first index on ties
+  float mv = -INFINITY;
+  int mi = V;
+  for (int j = j0; j < j1; ++j) {
+    const float y = val(j);
+    if (y > mv) { mv = y; mi = j; }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, mv, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, mi, o);
+    if (ov > mv || (ov == mv && oi < mi)) { mv = ov; mi = oi; }
+  }
+  if (lane == 0) { s_v[w] = mv; s_i[w] = mi; }
+  if (t == 0) s_pick = V;
+  __syncthreads();
+  if (w == 0) {
+    mv = s_v[lane];
+    mi = s_i[lane];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, mv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, mi, o);
+      if (ov > mv || (ov == mv && oi < mi)) { mv = ov; mi = oi; }
+    }
+    if (lane == 0) { s_v[0] = mv; s_i[0] = mi; }
+  }
+  __syncthreads();
+  if (!sample) {
+    if (t == 0) *out = min(s_i[0], V - 1);
+    return;
+  }
+  const float m = s_v[0];
+  float loc = 0.f;
+  for (int j = j0; j < j1; ++j) loc += expf(val(j) - m);
+  // exclusive prefix of the runs' sums in thread order
+  float inc = loc;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float x = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += x;
+  }
+  if (lane == 31) s_sum[w] = inc;
+  __syncthreads();
+  if (w == 0) {
+    float ws = s_sum[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float x = __shfl_up_sync(0xffffffffu, ws, o);
+      if (lane >= o) ws += x;
+    }
+    s_sum[lane] = ws;  // inclusive sum up to warp `lane`
+  }
+  __syncthreads();
+  const float total = s_sum[31];
+  const float target = *u * total;
+  float c = (w > 0 ? s_sum[w - 1] : 0.f) + (inc - loc);
+  for (int j = j0; j < j1; ++j) {
+    c += expf(val(j) - m);
+    if (c > target) {
+      atomicMin(&s_pick, j);
+      break;
+    }
+  }
+  __syncthreads();
+  if (t == 0) *out = min(s_pick, V - 1);
+}
+
 }  // namespace
+
+int rows_pick(const float* z, int V, int sample, float temp, const float* u, int* out, cudaStream_t st) {
+  return (int)launch_k(pick_kernel, dim3(1), dim3(kPickThreads), 0, st, z, V, sample, temp, u, out);
+}
 
 int rows_embed(const int* tok, int n, const float* E, int V, int d, float* x, int* err, cudaStream_t st) {
   return (int)launch_k(embed_kernel, dim3(row_grid(n)), dim3(kRowWarps * 32), 0, st, tok, n, E, V, d, x, err);

@@ -23,6 +23,8 @@ int rows_ce_combine(const float2* part, const float* zt, const int* tgt, int n, 
 int rows_loss_mean(const float* loss_row, const int* tgt, int n, float* out, float* inv_count, cudaStream_t st);
 int rows_convert(const float* src, long rows, int cols, long src_ld, bf16* dh, bf16* dl, long dst_ld,
                  cudaStream_t st);
+// next token from logits z[V]: sample = 0 greedy (first largest), 1 inverse CDF of softmax(z / temp) at *u
+int rows_pick(const float* z, int V, int sample, float temp, const float* u, int* out, cudaStream_t st);
 int rows_attn_rowdot(const bf16* doh, const bf16* dol, const bf16* oh, const bf16* ol, int n, int H, int dh, float* D,
                      cudaStream_t st);
 

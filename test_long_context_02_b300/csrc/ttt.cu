@@ -85,6 +85,7 @@ struct ttt_ctx {
   float *dy = nullptr, *dxn = nullptr, *dh32 = nullptr, *D = nullptr, *dq = nullptr, *dk = nullptr, *dv = nullptr;
   Pair dy16, da, dh16, do16, dqkv;
   float* sa_s = nullptr;     // dual-MLP: static pre-activations [S][b][f]
+  float* zdec = nullptr;     // decoding: one row of logits [V]
   Pair us, da_s;             // dual-MLP: static GELU output and its gradient [b][f]
   // host whole-sequence entry point: device staging of tokens and losses (grown on demand)
   int* seq_tok = nullptr;
@@ -181,12 +182,12 @@ bool attn_maps(AttnMaps* m, const Pair& q, const Pair& kr, const Pair& vr, const
 // Kernel classes timed by the optional profiler (names exported by ttt_profile_read).
 enum Cls : int {
   K_GEMM_QKV, K_ATTN_FWD, K_GEMM_O, K_GEMM_UP, K_GEMM_DOWN, K_CE_FWD, K_CE_BWD, K_LM_DX, K_MLP_DX, K_DW_SGD,
-  K_ATTN_DX, K_ATTN_DQ, K_ATTN_DKV, K_RMSNORM, K_ROPE, K_COMMIT, K_MISC, K_NCLS
+  K_ATTN_DX, K_ATTN_BWD, K_RMSNORM, K_ROPE, K_COMMIT, K_MISC, K_NCLS
 };
 const char* const kClsName[K_NCLS] = {
     "gemm_qkv", "attn_fwd", "gemm_o_resid", "gemm_up_gelu", "gemm_down_resid", "lmhead_ce_fwd",
-    "lmhead_ce_bwd", "lmhead_dx", "gemm_mlp_dx", "gemm_dw_sgd", "gemm_attn_dx", "attn_bwd_dq",
-    "attn_bwd_dkv", "rmsnorm", "rope", "kv_commit", "misc"};
+    "lmhead_ce_bwd", "lmhead_dx", "gemm_mlp_dx", "gemm_dw_sgd", "gemm_attn_dx", "attn_bwd",
+    "rmsnorm", "rope", "kv_commit", "misc"};
 
 cudaEvent_t next_event(ttt_ctx* c) {
   if (c->ev_used == c->ev_pool.size()) {
@@ -239,32 +240,38 @@ double tile_pairs(long pos0, int n, int k) {
   return t;
 }
 
-// Forward of block l over n rows at absolute positions pos0..pos0+n-1.  Frozen
-// blocks update the residual stream xin in place; trainable blocks (si >= 0)
-// keep what their backward needs in the suffix buffers and write xout.
-int layer_forward(ttt_ctx* c, Seq& sq_, int l, int si, int n, long pos0, float* xin, float* xout,
-                  const float* cs, const float* sn) {
+// Forward of block l over the n chunk rows r0 .. r0+n-1 (absolute positions
+// pos0+r0 ..., pos0 = the chunk's first position).  Blocks run with save =
+// false (the frozen blocks, and the trainable ones during decoding) update the
+// residual stream in place through the prefix-pass buffers; trainable blocks
+// run with save = true (r0 = 0) keep what their backward needs in the suffix
+// buffers and write xout.  si >= 0 selects the sequence's fast weights.
+// xin / xout and the angle tables cs / sn point at row r0.
+int layer_forward(ttt_ctx* c, Seq& sq_, int l, int si, bool save, int n, int r0, long pos0, float* xin,
+                  float* xout, const float* cs, const float* sn) {
   cudaStream_t st = c->st;
   const int d = c->d, H = c->H, dh = c->dh, f = c->f, k = c->k, b = c->b, R = c->R;
-  const bool suf = si >= 0, sp = c->split;
+  const bool fast = si >= 0, suf = fast && save, sp = c->split;
   const double nn = n, dd = d, ff = f;
   const double ops = sp ? 3.0 : 1.0, eb = sp ? 4.0 : 2.0;
+  const long ro = (long)r0 * d, rf = (long)r0 * f;
   float* hbuf = suf ? c->sh + (long)si * b * d : xin;
-  Pair xn_a = c->xn;
-  Pair qb = suf ? c->sq.at((long)si * b * d) : c->q;
-  Pair ob = suf ? c->so.at((long)si * b * d) : c->o;
-  Pair xn_m = suf ? c->sxm.at((long)si * b * d) : c->xn;
-  Pair ub = suf ? c->su.at((long)si * b * f) : c->u;
-  Pair ko = c->kown.at((long)l * R * d), vo = c->vown.at((long)l * R * d);
+  Pair xn_a = c->xn.at(ro);
+  Pair q0 = suf ? c->sq.at((long)si * b * d) : c->q;  // row 0 of the chunk's queries / outputs
+  Pair o0 = suf ? c->so.at((long)si * b * d) : c->o;
+  Pair xn_m = suf ? c->sxm.at((long)si * b * d) : c->xn.at(ro);
+  Pair ub = suf ? c->su.at((long)si * b * f) : c->u.at(rf);
+  Pair ko0 = c->kown.at((long)l * R * d), vo0 = c->vown.at((long)l * R * d);
   Pair kr = sq_.ring_k.at((long)l * k * d), vr = sq_.ring_v.at((long)l * k * d);
 
   RUN(K_RMSNORM, 1, 0, 0, nn * dd * (4 + eb),
       rows_rmsnorm(xin, c->gains + (long)(2 * l) * d, c->cfg.rms_eps, n, d, xn_a.hi, xn_a.lo,
                    suf ? c->srs_a + (long)si * b : nullptr, st));
+  Pair qw = q0.at(ro), kw = ko0.at(ro), vw = vo0.at(ro);
   if (qkv_rope_bn(dh, d, sp)) {  // RoPE and the q / own k / own v writes fused into the product's epilogue
     GemmArgs g;
     g.M = n; g.N = 3 * d; g.K = d; g.err = c->derr;
-    g.rq_h = qb.hi; g.rq_l = qb.lo; g.rk_h = ko.hi; g.rk_l = ko.lo; g.rv_h = vo.hi; g.rv_l = vo.lo;
+    g.rq_h = qw.hi; g.rq_l = qw.lo; g.rk_h = kw.hi; g.rk_l = kw.lo; g.rv_h = vw.hi; g.rv_l = vw.lo;
     g.rcs = cs; g.rsn = sn; g.rd = d;
     RUN(K_GEMM_QKV, 1, 6 * nn * dd * dd, 6 * nn * dd * dd * ops, 0,
         gemm_qkv_rope(opnd(xn_a, d, 0), opnd(c->Wqkv.at((long)l * d * 3 * d), 3 * d, 1), g, dh, sp, st));
@@ -275,18 +282,19 @@ int layer_forward(ttt_ctx* c, Seq& sq_, int l, int si, int n, long pos0, float* 
     RUN(K_GEMM_QKV, 1, 6 * nn * dd * dd, 6 * nn * dd * dd * ops, 0,
         gemm_run(EPI_F32, opnd(xn_a, d, 0), opnd(c->Wqkv.at((long)l * d * 3 * d), 3 * d, 1), g, sp, st));
     RUN(K_ROPE, 1, 0, 0, nn * dd * (12 + 3 * eb),
-        rows_rope_qkv(c->qkv, cs, sn, n, H, dh, qb.hi, qb.lo, ko.hi, ko.lo, vo.hi, vo.lo, st));
+        rows_rope_qkv(c->qkv, cs, sn, n, H, dh, qw.hi, qw.lo, kw.hi, kw.lo, vw.hi, vw.lo, st));
   }
-  {
+  {  // queries r0 .. r0+n-1 over the cache and own keys 0 .. r0+n-1 (tiles before r0's are skipped)
+    const int na = r0 + n;
     AttnMaps m;
-    if (!attn_maps(&m, qb, kr, vr, ko, vo, n, d, k)) return fail(c, TTT_ERR_CUDA, "attention tensor maps");
+    if (!attn_maps(&m, q0, kr, vr, ko0, vo0, na, d, k)) return fail(c, TTT_ERR_CUDA, "attention tensor maps");
     AttnArgs a;
-    a.n = n; a.H = H; a.dh = dh; a.window = k; a.pos0 = pos0;
+    a.n = na; a.H = H; a.dh = dh; a.window = k; a.pos0 = pos0; a.qt0 = r0 / 128;
     a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)dh));
-    a.o_hi = ob.hi; a.o_lo = ob.lo; a.ldo = d;
+    a.o_hi = o0.hi; a.o_lo = o0.lo; a.ldo = d;
     a.lse = suf ? c->slse + (long)si * H * b : nullptr;
     a.err = c->derr;
-    RUN(K_ATTN_FWD, 1, 4 * dd * window_pairs(pos0, n, k), 4 * dd * tile_pairs(pos0, n, k) * ops, 0,
+    RUN(K_ATTN_FWD, 1, 4 * dd * window_pairs(pos0 + r0, n, k), 4 * dd * tile_pairs(pos0, na, k) * ops, 0,
         attn_fwd_run(m, a, sp, st));
   }
   {
@@ -294,7 +302,7 @@ int layer_forward(ttt_ctx* c, Seq& sq_, int l, int si, int n, long pos0, float* 
     g.M = n; g.N = d; g.K = d;
     g.out32 = hbuf; g.ldo32 = d; g.resid = xin; g.ldr = d; g.err = c->derr; g.allow_ksplit = true;
     RUN(K_GEMM_O, 1, 2 * nn * dd * dd, 2 * nn * dd * dd * ops, 0,
-        gemm_run(EPI_RESID, opnd(ob, d, 0), opnd(c->Wo.at((long)l * d * d), d, 1), g, sp, st));
+        gemm_run(EPI_RESID, opnd(o0.at(ro), d, 0), opnd(c->Wo.at((long)l * d * d), d, 1), g, sp, st));
   }
   RUN(K_RMSNORM, 1, 0, 0, nn * dd * (4 + eb),
       rows_rmsnorm(hbuf, c->gains + (long)(2 * l + 1) * d, c->cfg.rms_eps, n, d, xn_m.hi, xn_m.lo,
@@ -304,7 +312,7 @@ int layer_forward(ttt_ctx* c, Seq& sq_, int l, int si, int n, long pos0, float* 
     g.M = n; g.N = f; g.K = d;
     g.out32 = suf ? c->sa + (long)si * b * f : nullptr;  // pre-activation kept for GELU' only when trainable
     g.ldo32 = f; g.oh = ub.hi; g.ol = ub.lo; g.ldo = f; g.err = c->derr;
-    Pair w = suf ? sq_.up16.at((long)si * d * f) : c->Wup.at((long)l * d * f);
+    Pair w = fast ? sq_.up16.at((long)si * d * f) : c->Wup.at((long)l * d * f);
     RUN(K_GEMM_UP, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 0,
         gemm_run(EPI_GELU, opnd(xn_m, d, 0), opnd(w, f, 1), g, sp, st));
   }
@@ -312,14 +320,15 @@ int layer_forward(ttt_ctx* c, Seq& sq_, int l, int si, int n, long pos0, float* 
     GemmArgs g;
     g.M = n; g.N = d; g.K = f;
     g.out32 = xout; g.ldo32 = d; g.resid = hbuf; g.ldr = d; g.err = c->derr; g.allow_ksplit = true;
-    Pair w = suf ? sq_.down16.at((long)si * f * d) : c->Wdown.at((long)l * f * d);
+    Pair w = fast ? sq_.down16.at((long)si * f * d) : c->Wdown.at((long)l * f * d);
     RUN(K_GEMM_DOWN, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 0,
         gemm_run(EPI_RESID, opnd(ub, f, 0), opnd(w, d, 1), g, sp, st));
   }
-  if (suf && c->dual) {  // the frozen static MLP of a trainable block, on the same normalised input
+  if (fast && c->dual) {  // the frozen static MLP of a trainable block, on the same normalised input
+    Pair usb = c->us.at(rf);
     GemmArgs g;
     g.M = n; g.N = f; g.K = d;
-    g.out32 = c->sa_s + (long)si * b * f; g.ldo32 = f; g.oh = c->us.hi; g.ol = c->us.lo; g.ldo = f;
+    g.out32 = suf ? c->sa_s + (long)si * b * f : nullptr; g.ldo32 = f; g.oh = usb.hi; g.ol = usb.lo; g.ldo = f;
     g.err = c->derr;
     RUN(K_GEMM_UP, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 0,
         gemm_run(EPI_GELU, opnd(xn_m, d, 0), opnd(c->Wup_s.at((long)si * d * f), f, 1), g, sp, st));
@@ -327,7 +336,7 @@ int layer_forward(ttt_ctx* c, Seq& sq_, int l, int si, int n, long pos0, float* 
     g2.M = n; g2.N = d; g2.K = f;
     g2.out32 = xout; g2.ldo32 = d; g2.resid = xout; g2.ldr = d; g2.err = c->derr; g2.allow_ksplit = true;
     RUN(K_GEMM_DOWN, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 0,
-        gemm_run(EPI_RESID, opnd(c->us, f, 0), opnd(c->Wdown_s.at((long)si * f * d), d, 1), g2, sp, st));
+        gemm_run(EPI_RESID, opnd(usb, f, 0), opnd(c->Wdown_s.at((long)si * f * d), d, 1), g2, sp, st));
   }
   return TTT_OK;
 }
@@ -347,7 +356,7 @@ int prefix_pass(ttt_ctx* c, int s, const int* tok, int n, long pos0) {
   RUN(K_MISC, 1, 0, 0, nn * dd * 8, rows_embed(tok, n, c->E, c->V, d, c->xp, c->derr, st));
   RUN(K_ROPE, 1, 0, 0, nn * dh * 4, rows_rope_table(pos0, n, dh, c->inv_freq, c->cs, c->sn, st));
   for (int l = 0; l < P0; ++l) {
-    const int r = layer_forward(c, sq_, l, -1, n, pos0, c->xp, c->xp, c->cs, c->sn);
+    const int r = layer_forward(c, sq_, l, -1, false, n, 0, pos0, c->xp, c->xp, c->cs, c->sn);
     if (r != TTT_OK) return r;
   }
   if (P0 > 0) {
@@ -393,7 +402,7 @@ int suffix_step(ttt_ctx* c, int s, int row, const int* tok, int n, const int* ne
     const int si = l - P0;
     float* xin = si == 0 ? c->xp + (long)row * d : c->sx + (long)si * b * d;
     float* xout = (l + 1 < L) ? c->sx + (long)(si + 1) * b * d : c->x;
-    const int r = layer_forward(c, sq_, l, si, n, pos0, xin, xout, cs, sn);
+    const int r = layer_forward(c, sq_, l, si, true, n, 0, pos0, xin, xout, cs, sn);
     if (r != TTT_OK) return r;
   }
   // final norm + LM head + cross-entropy statistics
@@ -517,8 +526,8 @@ int suffix_step(ttt_ctx* c, int s, int row, const int* tok, int n, const int* ne
       ba.dv = c->dv;
       ba.ldg = d;
       ba.scale = (float)(1.0 / std::sqrt((double)dh));
-      RUN(K_ATTN_DQ, 1, 4 * dd * pairs, 6 * dd * tpairs * ops, 0, attn_bwd_run(m, ba, sp, st, 1));
-      RUN(K_ATTN_DKV, 1, 4 * dd * own_pairs, 8 * dd * own_tile_pairs * ops, 0, attn_bwd_run(m, ba, sp, st, 2));
+      RUN(K_ATTN_BWD, 1, 4 * dd * (pairs + own_pairs), (6 * dd * tpairs + 8 * dd * own_tile_pairs) * ops, 0,
+          attn_bwd_run(m, ba, sp, st, 0));
     }
     RUN(K_ROPE, 1, 0, 0, nn * dd * (12 + 3 * eb),
         rows_rope_bwd(c->dq, c->dk, c->dv, cs, sn, n, H, dh, c->dqkv.hi, c->dqkv.lo, st));
@@ -651,6 +660,7 @@ extern "C" int ttt_create(const ttt_config* cfg, void* cuda_stream, ttt_ctx** ou
   c->dh16 = palloc(c, b * d, ok);
   c->do16 = palloc(c, b * d, ok);
   c->dqkv = palloc(c, b * 3 * d, ok);
+  c->zdec = dalloc<float>(c, V, ok);
   if (c->dual) {
     c->sa_s = dalloc<float>(c, S * b * f, ok);
     c->us = palloc(c, b * f, ok);
@@ -828,22 +838,101 @@ extern "C" int ttt_prefill_chunk(ttt_ctx* c, const int32_t* tokens, int32_t n, c
   return ttt_sync(c);
 }
 
-extern "C" int ttt_prefill_sequence_dev(ttt_ctx* c, const int32_t* d_tokens, int32_t T, float* d_losses) {
-  if (!c || !d_tokens || !d_losses || T < 1) return TTT_ERR_ARG;
-  if (!c->loaded) return fail(c, TTT_ERR_STATE, "weights not loaded");
+namespace {
+// Sequence s over T tokens (device ids): the frozen blocks run ahead over groups of
+// G chunks, the trainable blocks step chunk by chunk; losses[ceil(T/b)] (device).
+int prefill_one(ttt_ctx* c, int s, const int32_t* seq, int T, float* losses) {
   const int b = c->b;
   const int nc = (T + b - 1) / b;
   for (int g0 = 0; g0 < nc; g0 += c->G) {  // one frozen-prefix pass per group of G chunks
     const int g1 = std::min(nc, g0 + c->G);
     const int t0 = g0 * b, t1 = std::min(T, g1 * b);
-    for (int s = 0; s < c->B; ++s) {
-      const int32_t* seq = d_tokens + (long)s * T;
-      int r = prefix_pass(c, s, seq + t0, t1 - t0, c->seqs[s].pos);
+    int r = prefix_pass(c, s, seq + t0, t1 - t0, c->seqs[s].pos);
+    if (r != TTT_OK) return r;
+    for (int ci = g0; ci < g1; ++ci) {
+      const int s0 = ci * b, n = std::min(b, T - s0);
+      const int32_t* nx = (s0 + n < T) ? seq + s0 + n : c->minus1;
+      r = suffix_step(c, s, s0 - t0, seq + s0, n, nx, losses + ci);
       if (r != TTT_OK) return r;
-      for (int ci = g0; ci < g1; ++ci) {
-        const int s0 = ci * b, n = std::min(b, T - s0);
-        const int32_t* nx = (s0 + n < T) ? seq + s0 + n : c->minus1;
-        r = suffix_step(c, s, s0 - t0, seq + s0, n, nx, d_losses + (long)s * nc + ci);
+    }
+  }
+  return TTT_OK;
+}
+}  // namespace
+
+extern "C" int ttt_prefill_sequence_dev(ttt_ctx* c, const int32_t* d_tokens, int32_t T, float* d_losses) {
+  if (!c || !d_tokens || !d_losses || T < 1) return TTT_ERR_ARG;
+  if (!c->loaded) return fail(c, TTT_ERR_STATE, "weights not loaded");
+  const int nc = (T + c->b - 1) / c->b;
+  for (int s = 0; s < c->B; ++s) {
+    const int r = prefill_one(c, s, d_tokens + (long)s * T, T, d_losses + (long)s * nc);
+    if (r != TTT_OK) return r;
+  }
+  return TTT_OK;
+}
+
+namespace {
+// Logits of one row of the final normalised hidden state: z[V] = xf_row . W_lm.
+int logits_row(ttt_ctx* c, const Pair& xf_row, float* z) {
+  const double dd = c->d, VV = c->V;
+  GemmArgs g;
+  g.M = 1; g.N = c->V; g.K = c->d;
+  g.out32 = z; g.ldo32 = c->V; g.err = c->derr;
+  RUN(K_CE_FWD, 1, 2 * dd * VV, 2 * dd * VV * (c->split ? 3 : 1), 0,
+      gemm_run(EPI_F32, opnd(xf_row, c->d, 0), opnd(c->Wlm, c->V, 1), g, c->split, c->st));
+  return TTT_OK;
+}
+}  // namespace
+
+extern "C" int ttt_decode_dev(ttt_ctx* c, const int32_t* d_prompt, int32_t T, int32_t n_new, int32_t sample,
+                              float temp, const float* d_u, int32_t* d_out, float* d_prefill_losses,
+                              float* d_gen_losses, float* d_logits) {
+  if (!c || !d_prompt || !d_out || !d_prefill_losses || T < 1 || n_new < 0) return TTT_ERR_ARG;
+  if ((sample != 0 && sample != 1) || (sample && (!d_u || !(temp > 0.f)))) return TTT_ERR_ARG;
+  if (n_new >= c->b && !d_gen_losses) return TTT_ERR_ARG;
+  if (!c->loaded) return fail(c, TTT_ERR_STATE, "weights not loaded");
+  cudaStream_t st = c->st;
+  const int b = c->b, L = c->L, P0 = c->L - c->S, d = c->d, dh = c->dh, V = c->V;
+  const int ncp = (T + b - 1) / b, ncg = n_new / b;
+  const double dd = d;
+  for (int s = 0; s < c->B; ++s) {
+    Seq& sq_ = c->seqs[s];
+    const int32_t* prompt = d_prompt + (long)s * T;
+    int32_t* out = d_out + (long)s * (n_new + 1);
+    const float* u = d_u ? d_u + (long)s * (n_new + 1) : nullptr;
+    auto zrow = [&](int i) { return d_logits ? d_logits + ((long)s * (n_new + 1) + i) * V : c->zdec; };
+    // the prompt goes through the chunked inner loop; its last position has no target
+    int r = prefill_one(c, s, prompt, T, d_prefill_losses + (long)s * ncp);
+    if (r != TTT_OK) return r;
+    // the first token comes from the prompt's last position, as the last prompt chunk's
+    // forward computed it (before that chunk's update): the final hidden rows are still in xf
+    const int nl = T - (ncp - 1) * b;
+    r = logits_row(c, c->xf.at((long)(nl - 1) * d), zrow(0));
+    if (r != TTT_OK) return r;
+    RUN(K_MISC, 1, 0, 0, (double)V * 4, rows_pick(zrow(0), V, sample, temp, u, out, st));
+    for (int i = 0; i < n_new; ++i) {
+      const int rr = i % b;           // row of the token in its generated chunk
+      const long pos0 = sq_.pos;      // first position of that chunk
+      if (rr == 0) RUN(K_ROPE, 1, 0, 0, (double)b * dh * 4, rows_rope_table(pos0, b, dh, c->inv_freq, c->cs, c->sn, st));
+      // one-token forward with the chunk's starting fast weights; its keys/values go to row
+      // rr of the chunk's own buffers, the window cache is untouched until the chunk's step
+      float* x = c->xp + (long)rr * d;
+      RUN(K_MISC, 1, 0, 0, dd * 8, rows_embed(out + i, 1, c->E, V, d, x, c->derr, st));
+      for (int l = 0; l < L; ++l) {
+        r = layer_forward(c, sq_, l, l >= P0 ? l - P0 : -1, false, 1, rr, pos0, x, x, c->cs + (long)rr * (dh / 2),
+                          c->sn + (long)rr * (dh / 2));
+        if (r != TTT_OK) return r;
+      }
+      Pair xf = c->xf.at((long)rr * d);
+      RUN(K_RMSNORM, 1, 0, 0, dd * 8,
+          rows_rmsnorm(x, c->gains + (long)(2 * L) * d, c->cfg.rms_eps, 1, d, xf.hi, xf.lo, nullptr, st));
+      r = logits_row(c, xf, zrow(i + 1));
+      if (r != TTT_OK) return r;
+      RUN(K_MISC, 1, 0, 0, (double)V * 4, rows_pick(zrow(i + 1), V, sample, temp, u ? u + i + 1 : nullptr, out + i + 1, st));
+      if (rr == b - 1) {  // a complete generated chunk takes one inner-loop step; its last target is the pick above
+        const int32_t* ids = out + i - (b - 1);
+        r = prefix_pass(c, s, ids, b, pos0);
+        if (r == TTT_OK) r = suffix_step(c, s, 0, ids, b, out + i + 1, d_gen_losses + (long)s * ncg + i / b);
         if (r != TTT_OK) return r;
       }
     }
@@ -928,6 +1017,85 @@ extern "C" int ttt_get_window(ttt_ctx* c, int32_t seq, int32_t layer, float* k_o
     }
   }
   return TTT_OK;
+}
+
+// ------------------------------------------------------------------ state export / import
+// One sequence's resumable state, as raw bytes: a header, the fp32 fast
+// weights, then the window cache exactly as the device holds it (bf16 bits,
+// remainders too in the fp32 mode).  The bf16 shadows of the fast weights are
+// not stored: import derives them with the rounding the SGD step uses.
+namespace {
+struct StateHeader {
+  char magic[8];  // "TTTSTAT1"
+  int32_t L, S, d, f, k, split, dual, pad;
+  int64_t pos;
+};
+static_assert(sizeof(StateHeader) == 48, "state header layout");
+
+size_t state_parts(const ttt_ctx* c, size_t* fw, size_t* ring) {
+  *fw = (size_t)c->S * c->d * c->f * sizeof(float);                  // one of W_up, W_down
+  *ring = (size_t)c->L * c->k * c->d * sizeof(bf16);                 // one of K, V (hi or lo)
+  return sizeof(StateHeader) + 2 * *fw + (c->split ? 4 : 2) * *ring;
+}
+}  // namespace
+
+extern "C" int64_t ttt_state_bytes(const ttt_ctx* c) {
+  if (!c) return -1;
+  size_t fw, ring;
+  return (int64_t)state_parts(c, &fw, &ring);
+}
+
+extern "C" int ttt_export_state(ttt_ctx* c, int32_t seq, void* buf, size_t bytes) {
+  if (!c || !buf || seq < 0 || seq >= c->B) return TTT_ERR_ARG;
+  size_t fw, ring;
+  if (bytes != state_parts(c, &fw, &ring)) return fail(c, TTT_ERR_ARG, "state buffer size");
+  cudaError_t e = cudaStreamSynchronize(c->st);
+  if (e != cudaSuccess) return fail(c, TTT_ERR_CUDA, cudaGetErrorString(e));
+  const Seq& s = c->seqs[seq];
+  StateHeader h{};
+  std::memcpy(h.magic, "TTTSTAT1", 8);
+  h.L = c->L; h.S = c->S; h.d = c->d; h.f = c->f; h.k = c->k; h.split = c->split; h.dual = c->dual;
+  h.pos = s.pos;
+  uint8_t* p = static_cast<uint8_t*>(buf);
+  std::memcpy(p, &h, sizeof(h));
+  p += sizeof(h);
+  const void* src[6] = {s.up32, s.down32, s.ring_k.hi, s.ring_v.hi, s.ring_k.lo, s.ring_v.lo};
+  const size_t len[6] = {fw, fw, ring, ring, ring, ring};
+  for (int i = 0; i < (c->split ? 6 : 4); ++i) {
+    e = cudaMemcpy(p, src[i], len[i], cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail(c, TTT_ERR_CUDA, cudaGetErrorString(e));
+    p += len[i];
+  }
+  return TTT_OK;
+}
+
+extern "C" int ttt_import_state(ttt_ctx* c, int32_t seq, const void* buf, size_t bytes) {
+  if (!c || !buf || seq < 0 || seq >= c->B) return TTT_ERR_ARG;
+  if (!c->loaded) return fail(c, TTT_ERR_STATE, "weights not loaded");
+  size_t fw, ring;
+  if (bytes != state_parts(c, &fw, &ring)) return fail(c, TTT_ERR_ARG, "state buffer size");
+  StateHeader h;
+  std::memcpy(&h, buf, sizeof(h));
+  if (std::memcmp(h.magic, "TTTSTAT1", 8) != 0 || h.L != c->L || h.S != c->S || h.d != c->d || h.f != c->f ||
+      h.k != c->k || h.split != (int)c->split || h.dual != (int)c->dual || h.pos < 0)
+    return fail(c, TTT_ERR_ARG, "state was exported from a context of another shape");
+  cudaError_t e = cudaStreamSynchronize(c->st);
+  if (e != cudaSuccess) return fail(c, TTT_ERR_CUDA, cudaGetErrorString(e));
+  Seq& s = c->seqs[seq];
+  const uint8_t* p = static_cast<const uint8_t*>(buf) + sizeof(h);
+  void* dst[6] = {s.up32, s.down32, s.ring_k.hi, s.ring_v.hi, s.ring_k.lo, s.ring_v.lo};
+  const size_t len[6] = {fw, fw, ring, ring, ring, ring};
+  for (int i = 0; i < (c->split ? 6 : 4); ++i) {
+    e = cudaMemcpy(dst[i], p, len[i], cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return fail(c, TTT_ERR_CUDA, cudaGetErrorString(e));
+    p += len[i];
+  }
+  const long S = c->S, d = c->d, f = c->f;
+  CK(rows_convert(s.up32, S * d, (int)f, f, s.up16.hi, s.up16.lo, f, c->st));
+  CK(rows_convert(s.down32, S * f, (int)d, d, s.down16.hi, s.down16.lo, d, c->st));
+  c->launches += 2;
+  s.pos = h.pos;
+  return ttt_sync(c);
 }
 
 extern "C" int ttt_reset(ttt_ctx* c) {

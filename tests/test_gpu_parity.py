@@ -86,6 +86,37 @@ def run_gpu_host_sequence(shape, tokens, blob):
     return losses, fw, pos
 
 
+def run_gpu_resumed(shape, tokens, blob):
+    """The per-chunk API in one context up to the middle chunk boundary, the state moved
+    (ttt_export_state / ttt_import_state) into a fresh context, the rest there."""
+    b, Tn = shape.chunk, len(tokens)
+    cut = (-(-Tn // b) // 2) * b
+
+    def chunks(m, lo, hi):
+        out = []
+        for s in range(lo, hi, b):
+            n = min(b, Tn - s)
+            nxt = int(tokens[s + n]) if s + n < Tn else -1
+            out.append(float(m.prefill_chunk(tokens[s:s + n], [nxt])[0]))
+        return out
+
+    a = T.TTT.from_shape(shape)
+    a.load_weights(blob)
+    losses = chunks(a, 0, cut)
+    state = a.export_state(0)
+    a.close()
+    m = T.TTT.from_shape(shape)
+    m.load_weights(blob)
+    m.import_state(state, 0)
+    assert m.position == cut
+    assert m.export_state(0) == state  # the round trip is bit-exact
+    losses += chunks(m, cut, Tn)
+    fw = [m.fast_weights(0, i) for i in range(shape.n_trainable)]
+    pos = m.position
+    m.close()
+    return losses, fw, pos
+
+
 def check(shape, tokens, name, runner=None):
     blob = weight_blob(shape)
     cfg = O.Config.from_shape(shape)
@@ -194,3 +225,23 @@ def test_allocation_failure_reports_oom_and_leaves_the_process_usable():
     s = SHAPES["tiny"]
     tok = sequence_tokens(s)
     check(s.replace(seq_len=256), tok[:256], "tiny fp32 after an allocation failure")
+
+
+@pytest.mark.parametrize("name", ["dh96_ahead4", "fp32_dh64", "dual_dh64"])
+def test_state_export_import_resumes_the_sequence(name):
+    s = SMALL[name]
+    check(s, zipf_tokens(s.seq_len, s.vocab, seed=1000), name + " (resumed)", runner=run_gpu_resumed)
+
+
+def test_state_import_rejects_another_shape():
+    a = T.TTT.from_shape(SMALL["dh64"])
+    a.load_weights(weight_blob(SMALL["dh64"]))
+    state = a.export_state(0)
+    a.close()
+    other = SMALL["dh64"].replace(window=512)
+    m = T.TTT.from_shape(other)
+    m.load_weights(weight_blob(other))
+    with pytest.raises(T.TTTError) as e:
+        m.import_state(state + bytes(int(T.ttt_state_bytes(m._h)) - len(state)), 0)
+    assert e.value.code == T.TTT_ERR_ARG
+    m.close()
