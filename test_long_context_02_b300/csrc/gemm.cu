@@ -251,24 +251,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       bool ok = true;
       uint32_t issued = 0;  // bit s: stage s has a fill in flight or landed
       uint32_t iss_par = 0; // bit s: parity of that fill
-      // fp32 operand the epilogue reads (residual, GELU argument, fp32 weights): its tile is
-      // brought into L2 while the tile's mainloop runs, so the epilogue does not wait on HBM
-      constexpr bool kEpiIn = EPI == EPI_RESID || EPI == EPI_GELU_BWD || EPI == EPI_SGD;
-      const float* ein = EPI == EPI_RESID ? g.resid : (EPI == EPI_GELU_BWD ? g.aux : g.w32);
-      const long ldein = EPI == EPI_RESID ? g.ldr : (EPI == EPI_GELU_BWD ? g.ldaux : g.ldw);
-      const bool pf = kEpiIn && ein != nullptr && !(EPI == EPI_RESID && ks > 1) && (ldein & 3) == 0;
       for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
         const int t = u % ntiles, sl = u / ntiles;
         const int m0 = (t % mt) * BM, n0 = (t / mt) * BN;
         const int kb0 = (int)((long)sl * nk / ks), kb1 = (int)((long)(sl + 1) * nk / ks);
-        if (pf) {
-          const uint32_t bytes = (uint32_t)(min(BN, g.N - n0) * 4) & ~15u;
-          const int r1 = min(m0 + BM, g.M);
-          for (int r = m0; r < r1 && bytes; ++r) {
-            const float* a = ein + (long)r * ldein + n0;
-            if ((reinterpret_cast<uintptr_t>(a) & 15u) == 0) prefetch_l2(a, bytes);
-          }
-        }
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, g.err, DERR_TIMEOUT_PRODUCER)) {
             ok = false;

@@ -117,12 +117,6 @@ TTT_DEV void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x
       : "memory");
 }
 
-// Hint: bring `bytes` (a multiple of 16) at the 16-byte aligned global address p
-// into L2.  No data arrives anywhere else and nothing waits for it.
-TTT_DEV void prefetch_l2(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
 // ----------------------------------------------------------------- tcgen05
 TTT_DEV void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {  // whole warp
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),

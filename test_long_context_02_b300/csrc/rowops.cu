@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(128) rmsnorm_bwd_kernel(const float* __restric
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (row >= n) return;
   const long base = (long)row * d;
-  float a[NCH][8], b[NCH][8];
+  float a[NCH][8], b[NCH][8], q[NCH][8];  // dy, x and the residual of the row, all loads in flight at once
   float s = 0.f;
 #pragma unroll
   for (int i = 0; i < NCH; ++i) {
@@ -155,6 +155,12 @@ __global__ void __launch_bounds__(128) rmsnorm_bwd_kernel(const float* __restric
       float gg[8];
       load8(dy + base + c, a[i]);
       load8(x + base + c, b[i]);
+      if (resid) {
+        load8(resid + base + c, q[i]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) q[i][e] = 0.f;
+      }
       load8(g + c, gg);
 #pragma unroll
       for (int e = 0; e < 8; ++e) s += a[i][e] * gg[e] * b[i][e];
@@ -169,14 +175,8 @@ __global__ void __launch_bounds__(128) rmsnorm_bwd_kernel(const float* __restric
     if (c < d) {
       float gg[8], rr[8];
       load8(g + c, gg);
-      if (resid) {
-        load8(resid + base + c, rr);
-      } else {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) rr[e] = 0.f;
-      }
-#pragma unroll
-      for (int e = 0; e < 8; ++e) rr[e] += r * gg[e] * a[i][e] - b[i][e] * k;
+      for (int e = 0; e < 8; ++e) rr[e] = q[i][e] + (r * gg[e] * a[i][e] - b[i][e] * k);
       float4* o = reinterpret_cast<float4*>(out + base + c);
       o[0] = make_float4(rr[0], rr[1], rr[2], rr[3]);
       o[1] = make_float4(rr[4], rr[5], rr[6], rr[7]);
