@@ -153,7 +153,7 @@ def replica_tokens_per_s(world, steps, tokens_per_step, seconds):
 # DRAM bytes (read + write) of one steady-state launch (window full) of the attention
 # forward at the 760M shape, from `ncu --set full` captures of this kernel: the
 # frozen-block pass over 8192 queries, and a trainable block over one 1024-token chunk.
-ATTN_FWD_TRAFFIC_760M = {"pass": 126.13e6 + 14.71e6, "step": 59.84e6 + 0.81e6}
+ATTN_FWD_TRAFFIC_760M = {"pass": 126.13e6 + 14.74e6, "step": 59.84e6 + 0.55e6}
 
 
 def attn_fwd_traffic(shape, nc):

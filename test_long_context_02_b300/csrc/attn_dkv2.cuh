@@ -270,10 +270,13 @@ TTT_DEV void dkv2_body(const CUtensorMap* tQ, const CUtensorMap* tQl, const CUte
       const float* sd = sl + 128;
       float pv[64];
       tmem_ld64(trow + T_S + b0, pv);  // S^T row
+      const uint64_t sc2 = f32x2(sl2, sl2);
 #pragma unroll
-      for (int e = 0; e < 64; ++e) {
-        const float pr = ex2_approx(fmaf(pv[e], sl2, -sl[e]));
-        pv[e] = (full || (b0 + e >= c_lo && b0 + e <= c_hi)) ? pr : 0.f;
+      for (int e = 0; e < 64; e += 2) {  // pairs of query columns in packed f32x2 arithmetic
+        const float2 a = f32x2_split(ffma2(f32x2(pv[e], pv[e + 1]), sc2, f32x2(-sl[e], -sl[e + 1])));
+        const float p0 = ex2_approx(a.x), p1 = ex2_approx(a.y);
+        pv[e] = (full || (b0 + e >= c_lo && b0 + e <= c_hi)) ? p0 : 0.f;
+        pv[e + 1] = (full || (b0 + e + 1 >= c_lo && b0 + e + 1 <= c_hi)) ? p1 : 0.f;
       }
       {
         uint32_t hi[32], lo[32];
@@ -289,7 +292,13 @@ TTT_DEV void dkv2_body(const CUtensorMap* tQ, const CUtensorMap* tQl, const CUte
         float dp[32];
         tmem_ld32(trow + T_DP + (uint32_t)(b0 + 32 * c), dp);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) pv[32 * c + e] *= dp[e] - sd[32 * c + e];
+        for (int e = 0; e < 32; e += 2) {
+          const int i = 32 * c + e;
+          const float2 x = f32x2_split(fmul2(f32x2(pv[i], pv[i + 1]),
+                                             fadd2(f32x2(dp[e], dp[e + 1]), f32x2(-sd[i], -sd[i + 1]))));
+          pv[i] = x.x;
+          pv[i + 1] = x.y;
+        }
       }
       {
         uint32_t hi[32], lo[32];

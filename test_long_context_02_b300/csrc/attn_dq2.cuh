@@ -282,16 +282,20 @@ TTT_DEV void dq2_body(const CUtensorMap* tQ, const CUtensorMap* tQl, const CUten
       const float* sv = sd;
       const float* dp = sd + 64;
       uint32_t hi[32], lo[32];
+      // dS = P (dP - D), P = 2^(S scale_log2 - lse2): pairs of columns in packed f32x2
+      // arithmetic (each lane rounded as the scalar instruction would round it)
+      const uint64_t sc2 = f32x2(sl2, sl2), nl2 = f32x2(-lse2, -lse2), nd2 = f32x2(-Dr, -Dr);
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
-        float x[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int col = b0 + 2 * e + u;
-          float pr = ex2_approx(fmaf(sv[2 * e + u], sl2, -lse2));
-          if (!full) pr = (col >= c_lo && col <= c_hi) ? pr : 0.f;
-          x[u] = pr * (dp[2 * e + u] - Dr);
+        const float2 a = f32x2_split(ffma2(f32x2(sv[2 * e], sv[2 * e + 1]), sc2, nl2));
+        float p0 = ex2_approx(a.x), p1 = ex2_approx(a.y);
+        if (!full) {
+          const int col = b0 + 2 * e;
+          p0 = (col >= c_lo && col <= c_hi) ? p0 : 0.f;
+          p1 = (col + 1 >= c_lo && col + 1 <= c_hi) ? p1 : 0.f;
         }
+        const float2 xx = f32x2_split(fmul2(f32x2(p0, p1), fadd2(f32x2(dp[2 * e], dp[2 * e + 1]), nd2)));
+        const float x[2] = {xx.x, xx.y};
         __nv_bfloat162 t = __floats2bfloat162_rn(x[0], x[1]);
         hi[e] = *reinterpret_cast<uint32_t*>(&t);
         if (SPLIT) {

@@ -307,18 +307,31 @@ __global__ void ce_combine_kernel(const float2* __restrict__ part, const float* 
                                   float* __restrict__ loss_row) {
   pdl_wait();
   pdl_launch_dependents();
-  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  // one warp per row: lane i merges the (max, sum) pairs of tiles i, i+32, ..., then the warp merges the lanes
+  const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (r >= n) return;
-  float m = -INFINITY;
-  for (int i = 0; i < ntiles; ++i) m = fmaxf(m, part[(long)i * n + r].x);
-  float s = 0.f;
-  for (int i = 0; i < ntiles; ++i) {
+  float m = -INFINITY, s = 0.f;
+  for (int i = lane; i < ntiles; i += 32) {
     const float2 p = part[(long)i * n + r];
-    s += p.y * expf(p.x - m);
+    if (p.x > m) {
+      s = s * expf(m - p.x) + p.y;
+      m = p.x;
+    } else {
+      s += p.y * expf(p.x - m);
+    }
   }
-  const float l = m + logf(s);
-  lse[r] = l;
-  loss_row[r] = (tgt[r] >= 0) ? (l - zt[r]) : 0.f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float om = __shfl_xor_sync(0xffffffffu, m, o), os = __shfl_xor_sync(0xffffffffu, s, o);
+    const float mm = fmaxf(m, om);
+    s = (m == -INFINITY ? 0.f : s * expf(m - mm)) + (om == -INFINITY ? 0.f : os * expf(om - mm));
+    m = mm;
+  }
+  if (lane == 0) {
+    const float l = m + logf(s);
+    lse[r] = l;
+    loss_row[r] = (tgt[r] >= 0) ? (l - zt[r]) : 0.f;
+  }
 }
 
 // Mean over the rows with a target, fixed reduction order (bit-reproducible).
@@ -563,7 +576,8 @@ int rows_commit(const bf16* own, bf16* ring, long own_layer_stride, long ring_la
 
 int rows_ce_combine(const float2* part, const float* zt, const int* tgt, int n, int ntiles, float* lse,
                     float* loss_row, cudaStream_t st) {
-  return (int)launch_k(ce_combine_kernel, dim3((n + 127) / 128), dim3(128), 0, st, part, zt, tgt, n, ntiles, lse, loss_row);
+  return (int)launch_k(ce_combine_kernel, dim3(row_grid(n)), dim3(kRowWarps * 32), 0, st, part, zt, tgt, n, ntiles, lse,
+                       loss_row);
 }
 
 int rows_loss_mean(const float* loss_row, const int* tgt, int n, float* out, float* inv_count, cudaStream_t st) {

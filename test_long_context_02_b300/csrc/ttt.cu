@@ -76,6 +76,14 @@ struct ttt_ctx {
   float *cs = nullptr, *sn = nullptr;
   float *x = nullptr, *xp = nullptr, *qkv = nullptr;
   Pair xn, q, o, u;
+  // frozen-prefix pass outputs, double-buffered so the pass of the next group of chunks
+  // can run on a second stream while the current group's trainable steps read theirs
+  float* xpb[2] = {nullptr, nullptr};   // [R][d] residual stream after the frozen blocks (xpb[0] == xp)
+  float* csb[2] = {nullptr, nullptr};   // angle tables [R][dh/2] (csb[0] == cs, snb[0] == sn)
+  float* snb[2] = {nullptr, nullptr};
+  Pair sxn;                             // [b][d] normalised attention input of the trainable blocks
+  cudaStream_t st2 = nullptr;           // the frozen-prefix passes run ahead on this stream
+  cudaEvent_t ev_fork = nullptr, ev_pass[2] = {nullptr, nullptr}, ev_suf[2] = {nullptr, nullptr};
   Pair kown, vown;           // [L][R][d]
   float *sx = nullptr, *sh = nullptr, *srs_a = nullptr, *srs_m = nullptr, *slse = nullptr, *sa = nullptr;
   Pair sq, so, sxm, su;
@@ -248,15 +256,14 @@ double tile_pairs(long pos0, int n, int k) {
 // buffers and write xout.  si >= 0 selects the sequence's fast weights.
 // xin / xout and the angle tables cs / sn point at row r0.
 int layer_forward(ttt_ctx* c, Seq& sq_, int l, int si, bool save, int n, int r0, long pos0, float* xin,
-                  float* xout, const float* cs, const float* sn) {
-  cudaStream_t st = c->st;
+                  float* xout, const float* cs, const float* sn, cudaStream_t st) {
   const int d = c->d, H = c->H, dh = c->dh, f = c->f, k = c->k, b = c->b, R = c->R;
   const bool fast = si >= 0, suf = fast && save, sp = c->split;
   const double nn = n, dd = d, ff = f;
   const double ops = sp ? 3.0 : 1.0, eb = sp ? 4.0 : 2.0;
   const long ro = (long)r0 * d, rf = (long)r0 * f;
   float* hbuf = suf ? c->sh + (long)si * b * d : xin;
-  Pair xn_a = c->xn.at(ro);
+  Pair xn_a = suf ? c->sxn : c->xn.at(ro);
   Pair q0 = suf ? c->sq.at((long)si * b * d) : c->q;  // row 0 of the chunk's queries / outputs
   Pair o0 = suf ? c->so.at((long)si * b * d) : c->o;
   Pair xn_m = suf ? c->sxm.at((long)si * b * d) : c->xn.at(ro);
@@ -347,16 +354,16 @@ int layer_forward(ttt_ctx* c, Seq& sq_, int l, int si, bool save, int n, int r0,
 // those chunks then read their rows of c->xp.  The frozen blocks' keys/values
 // of all n tokens enter the window cache at the end of the pass (every query of
 // the pass has already read the cache).
-int prefix_pass(ttt_ctx* c, int s, const int* tok, int n, long pos0) {
+int prefix_pass(ttt_ctx* c, int s, const int* tok, int n, long pos0, cudaStream_t st, int buf) {
   Seq& sq_ = c->seqs[s];
-  cudaStream_t st = c->st;
+  float* xp = c->xpb[buf];
   const int d = c->d, dh = c->dh, k = c->k, R = c->R;
   const int P0 = c->L - c->S;
   const double nn = n, dd = d;
-  RUN(K_MISC, 1, 0, 0, nn * dd * 8, rows_embed(tok, n, c->E, c->V, d, c->xp, c->derr, st));
-  RUN(K_ROPE, 1, 0, 0, nn * dh * 4, rows_rope_table(pos0, n, dh, c->inv_freq, c->cs, c->sn, st));
+  RUN(K_MISC, 1, 0, 0, nn * dd * 8, rows_embed(tok, n, c->E, c->V, d, xp, c->derr, st));
+  RUN(K_ROPE, 1, 0, 0, nn * dh * 4, rows_rope_table(pos0, n, dh, c->inv_freq, c->csb[buf], c->snb[buf], st));
   for (int l = 0; l < P0; ++l) {
-    const int r = layer_forward(c, sq_, l, -1, false, n, 0, pos0, c->xp, c->xp, c->cs, c->sn);
+    const int r = layer_forward(c, sq_, l, -1, false, n, 0, pos0, xp, xp, c->csb[buf], c->snb[buf], st);
     if (r != TTT_OK) return r;
   }
   if (P0 > 0) {
@@ -377,7 +384,7 @@ int prefix_pass(ttt_ctx* c, int s, const int* tok, int n, long pos0) {
 // within the last prefix pass: tokens tok[n], next target next[1] (device).
 // Runs the trainable blocks forward, the loss, the backward through them with
 // the fused SGD step, and commits their keys/values; the position advances by n.
-int suffix_step(ttt_ctx* c, int s, int row, const int* tok, int n, const int* next, float* loss_out) {
+int suffix_step(ttt_ctx* c, int s, int row, const int* tok, int n, const int* next, float* loss_out, int buf = 0) {
   Seq& sq_ = c->seqs[s];
   cudaStream_t st = c->st;
   const int L = c->L, S = c->S, d = c->d, H = c->H, dh = c->dh, f = c->f, V = c->V, k = c->k, b = c->b, R = c->R;
@@ -392,17 +399,17 @@ int suffix_step(ttt_ctx* c, int s, int row, const int* tok, int n, const int* ne
   const double own_pairs = nn * (nn + 1) / 2;
   const int nq = (n + 127) / 128;
   const double own_tile_pairs = 128.0 * 128.0 * nq * (nq + 1) / 2;
-  const float* cs = c->cs + (long)row * (dh / 2);
-  const float* sn = c->sn + (long)row * (dh / 2);
+  const float* cs = c->csb[buf] + (long)row * (dh / 2);
+  const float* sn = c->snb[buf] + (long)row * (dh / 2);
 
   RUN(K_MISC, 1, 0, 0, nn * 8, rows_targets(tok, n, next, V, c->tgt, c->derr, st));
 
   // ------------------------------------------------------------------ forward
   for (int l = P0; l < L; ++l) {
     const int si = l - P0;
-    float* xin = si == 0 ? c->xp + (long)row * d : c->sx + (long)si * b * d;
+    float* xin = si == 0 ? c->xpb[buf] + (long)row * d : c->sx + (long)si * b * d;
     float* xout = (l + 1 < L) ? c->sx + (long)(si + 1) * b * d : c->x;
-    const int r = layer_forward(c, sq_, l, si, true, n, 0, pos0, xin, xout, cs, sn);
+    const int r = layer_forward(c, sq_, l, si, true, n, 0, pos0, xin, xout, cs, sn, st);
     if (r != TTT_OK) return r;
   }
   // final norm + LM head + cross-entropy statistics
@@ -623,6 +630,13 @@ extern "C" int ttt_create(const ttt_config* cfg, void* cuda_stream, ttt_ctx** ou
   c->sn = dalloc<float>(c, R * dh / 2, ok);
   c->x = dalloc<float>(c, b * d, ok);
   c->xp = dalloc<float>(c, R * d, ok);
+  c->xpb[0] = c->xp;
+  c->xpb[1] = dalloc<float>(c, R * d, ok);
+  c->csb[0] = c->cs;
+  c->snb[0] = c->sn;
+  c->csb[1] = dalloc<float>(c, R * dh / 2, ok);
+  c->snb[1] = dalloc<float>(c, R * dh / 2, ok);
+  c->sxn = palloc(c, b * d, ok);
   c->qkv = dalloc<float>(c, R * 3 * d, ok);
   c->xn = palloc(c, R * d, ok);
   c->q = palloc(c, R * d, ok);
@@ -670,6 +684,16 @@ extern "C" int ttt_create(const ttt_config* cfg, void* cuda_stream, ttt_ctx** ou
     ttt_destroy(c);
     return TTT_ERR_OOM;
   }
+  if (cudaStreamCreateWithFlags(&c->st2, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&c->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&c->ev_pass[0], cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&c->ev_pass[1], cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&c->ev_suf[0], cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&c->ev_suf[1], cudaEventDisableTiming) != cudaSuccess) {
+    cudaGetLastError();
+    ttt_destroy(c);
+    return TTT_ERR_CUDA;
+  }
   std::vector<double> invf(dh / 2);
   for (int i = 0; i < dh / 2; ++i) invf[i] = std::pow(g.rope_theta, -2.0 * i / (double)dh);
   int m1 = -1;
@@ -686,7 +710,11 @@ extern "C" int ttt_create(const ttt_config* cfg, void* cuda_stream, ttt_ctx** ou
 extern "C" void ttt_destroy(ttt_ctx* c) {
   if (!c) return;
   if (c->st) cudaStreamSynchronize(c->st);
+  if (c->st2) cudaStreamSynchronize(c->st2);
   cudaDeviceSynchronize();
+  if (c->st2) cudaStreamDestroy(c->st2);
+  for (cudaEvent_t e : {c->ev_fork, c->ev_pass[0], c->ev_pass[1], c->ev_suf[0], c->ev_suf[1]})
+    if (e) cudaEventDestroy(e);
   for (void* p : c->allocs) cudaFree(p);
   if (c->seq_tok) cudaFree(c->seq_tok);
   if (c->seq_loss) cudaFree(c->seq_loss);
@@ -811,7 +839,7 @@ extern "C" int ttt_prefill_chunk_dev(ttt_ctx* c, const int32_t* d_tokens, int32_
   if (n < 1 || n > c->b) return fail(c, TTT_ERR_ARG, "n outside 1..chunk");
   for (int s = 0; s < c->B; ++s) {
     const int32_t* tk = d_tokens + (long)s * n;
-    int r = prefix_pass(c, s, tk, n, c->seqs[s].pos);
+    int r = prefix_pass(c, s, tk, n, c->seqs[s].pos, c->st, 0);
     if (r == TTT_OK) r = suffix_step(c, s, 0, tk, n, d_next + s, d_loss + s);
     if (r != TTT_OK) return r;
   }
@@ -841,22 +869,62 @@ extern "C" int ttt_prefill_chunk(ttt_ctx* c, const int32_t* tokens, int32_t n, c
 namespace {
 // Sequence s over T tokens (device ids): the frozen blocks run ahead over groups of
 // G chunks, the trainable blocks step chunk by chunk; losses[ceil(T/b)] (device).
+// With more than one group, the frozen pass of group g+1 runs on the second stream
+// while group g's trainable steps run on the context stream: the pass outputs are
+// double-buffered, the steps of group g wait for pass g, and pass g+2 waits for the
+// steps of group g (the last readers of its buffer).  The two sides share no other
+// buffer: the steps touch only the trainable blocks' keys/values and window caches.
 int prefill_one(ttt_ctx* c, int s, const int32_t* seq, int T, float* losses) {
-  const int b = c->b;
-  const int nc = (T + b - 1) / b;
-  for (int g0 = 0; g0 < nc; g0 += c->G) {  // one frozen-prefix pass per group of G chunks
-    const int g1 = std::min(nc, g0 + c->G);
-    const int t0 = g0 * b, t1 = std::min(T, g1 * b);
-    int r = prefix_pass(c, s, seq + t0, t1 - t0, c->seqs[s].pos);
-    if (r != TTT_OK) return r;
+  const int b = c->b, G = c->G;
+  const int nc = (T + b - 1) / b, ng = (nc + G - 1) / G;
+  const long base = c->seqs[s].pos;
+  auto steps = [&](int g, int buf) -> int {
+    const int g0 = g * G, g1 = std::min(nc, g0 + G), t0 = g0 * b;
     for (int ci = g0; ci < g1; ++ci) {
       const int s0 = ci * b, n = std::min(b, T - s0);
       const int32_t* nx = (s0 + n < T) ? seq + s0 + n : c->minus1;
-      r = suffix_step(c, s, s0 - t0, seq + s0, n, nx, losses + ci);
+      const int r = suffix_step(c, s, s0 - t0, seq + s0, n, nx, losses + ci, buf);
       if (r != TTT_OK) return r;
     }
+    return TTT_OK;
+  };
+  auto pass = [&](int g, cudaStream_t st, int buf) -> int {
+    const int t0 = g * G * b, t1 = std::min(T, (g + 1) * G * b);
+    return prefix_pass(c, s, seq + t0, t1 - t0, base + t0, st, buf);
+  };
+  const bool overlap = ng > 1 && c->prof_mask == 0 && qkv_rope_bn(c->dh, c->d, c->split) != 0;
+  if (!overlap) {
+    for (int g = 0; g < ng; ++g) {
+      int r = pass(g, c->st, 0);
+      if (r == TTT_OK) r = steps(g, 0);
+      if (r != TTT_OK) return r;
+    }
+    return TTT_OK;
   }
-  return TTT_OK;
+  // the second stream starts after everything already enqueued on the context stream
+  CK(cudaEventRecord(c->ev_fork, c->st));
+  CK(cudaStreamWaitEvent(c->st2, c->ev_fork, 0));
+  auto ahead = [&](int g) -> int {
+    if (g >= 2) CK(cudaStreamWaitEvent(c->st2, c->ev_suf[g & 1], 0));
+    const int r = pass(g, c->st2, g & 1);
+    if (r != TTT_OK) return r;
+    CK(cudaEventRecord(c->ev_pass[g & 1], c->st2));
+    return TTT_OK;
+  };
+  int r = ahead(0);
+  for (int g = 0; g < ng && r == TTT_OK; ++g) {
+    if (g + 1 < ng) r = ahead(g + 1);
+    if (r != TTT_OK) break;
+    CK(cudaStreamWaitEvent(c->st, c->ev_pass[g & 1], 0));
+    r = steps(g, g & 1);
+    if (r != TTT_OK) break;
+    CK(cudaEventRecord(c->ev_suf[g & 1], c->st));
+  }
+  if (r != TTT_OK) {  // keep later work on the context stream behind whatever the second stream has queued
+    cudaEventRecord(c->ev_fork, c->st2);
+    cudaStreamWaitEvent(c->st, c->ev_fork, 0);
+  }
+  return r;
 }
 }  // namespace
 
@@ -920,7 +988,7 @@ extern "C" int ttt_decode_dev(ttt_ctx* c, const int32_t* d_prompt, int32_t T, in
       RUN(K_MISC, 1, 0, 0, dd * 8, rows_embed(out + i, 1, c->E, V, d, x, c->derr, st));
       for (int l = 0; l < L; ++l) {
         r = layer_forward(c, sq_, l, l >= P0 ? l - P0 : -1, false, 1, rr, pos0, x, x, c->cs + (long)rr * (dh / 2),
-                          c->sn + (long)rr * (dh / 2));
+                          c->sn + (long)rr * (dh / 2), st);
         if (r != TTT_OK) return r;
       }
       Pair xf = c->xf.at((long)rr * d);
@@ -931,7 +999,7 @@ extern "C" int ttt_decode_dev(ttt_ctx* c, const int32_t* d_prompt, int32_t T, in
       RUN(K_MISC, 1, 0, 0, (double)V * 4, rows_pick(zrow(i + 1), V, sample, temp, u ? u + i + 1 : nullptr, out + i + 1, st));
       if (rr == b - 1) {  // a complete generated chunk takes one inner-loop step; its last target is the pick above
         const int32_t* ids = out + i - (b - 1);
-        r = prefix_pass(c, s, ids, b, pos0);
+        r = prefix_pass(c, s, ids, b, pos0, c->st, 0);
         if (r == TTT_OK) r = suffix_step(c, s, 0, ids, b, out + i + 1, d_gen_losses + (long)s * ncg + i / b);
         if (r != TTT_OK) return r;
       }

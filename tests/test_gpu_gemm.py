@@ -75,6 +75,24 @@ def test_gemm_f32_layouts(M, N, K, a_mn, b_mn):
     assert rel(got, ref) < 2e-6, (M, N, K, a_mn, b_mn)
 
 
+# Shapes whose tile choice is 256 or 192 wide with at least two M tiles: the kernel then runs
+# as clusters of two CTAs on adjacent M tiles that share each B tile (each loads half of it
+# and multicasts it to both).  1152 rows give an odd tile count, so the second CTA of the
+# last pair computes a tile that lies wholly past M.
+@pytest.mark.parametrize("M,N,K", [(1152, 4096, 320), (1024, 6144, 256), (2048, 1536, 1024)])
+@pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 0), (1, 1)])
+def test_gemm_paired_ctas(M, N, K, a_mn, b_mn):
+    a, b, Aq, Bq = operands(M, N, K, a_mn, b_mn)
+    out = torch.full((M, N), float("nan"), dtype=torch.float32, device=dev)
+    err = errword()
+    T.gemm(T.EPI_F32, M, N, K, a, b, a_mn=a_mn, b_mn=b_mn, out32=out, ldo32=N, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    got = out.cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(got))
+    assert rel(got, Aq @ Bq.T) < 2e-6, (M, N, K, a_mn, b_mn)
+
+
 @pytest.mark.parametrize("a_mn,b_mn", [(0, 1), (1, 1), (0, 0)])
 def test_gemm_split_mode_fp32_accuracy(a_mn, b_mn):
     M, N, K = 200, 320, 384
