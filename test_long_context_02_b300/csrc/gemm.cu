@@ -187,12 +187,7 @@ TTT_DEV void load_f32_32(const float* p, float (&v)[32], int ncols) {
 constexpr int kGemmThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue (two per TMEM lane quadrant)
 constexpr int kXposeBytes = 8 * 32 * 33 * 4;  // elementwise epilogues: a 32 x 33 fp32 buffer per epilogue warp
 
-// MC: the grid runs as clusters of two CTAs on vertically adjacent tiles (same N
-// tile, same K range).  Each CTA loads its own A tile and HALF of the shared B
-// tile, multicasting that half into both CTAs' shared memory, so each SM reads
-// 2/3 of the operand bytes of a lone CTA from L2.  A stage is refilled only when
-// both CTAs' MMAs are done with it (their commits arrive on both empty barriers).
-template <int BN, bool SPLIT, int EPI, int DH, bool MC>
+template <int BN, bool SPLIT, int EPI, int DH>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tAl,
                 const __grid_constant__ CUtensorMap tB, const __grid_constant__ CUtensorMap tBl, const GemmArgs g) {
@@ -212,30 +207,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                               EPI == EPI_GELU_BWD || EPI == EPI_SGD;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int mt = (g.M + BM - 1) / BM, nt = (g.N + BN - 1) / BN;
+  const int mt = (g.M + BM - 1) / BM, nt = (g.N + BN - 1) / BN, ntiles = mt * nt;
   const int nk = (g.K + BK - 1) / BK;
-  // work unit u = (output tile, K slice u / tiles); slices > 1 only for the F32 /
-  // RESID epilogues, which then add their partial sums atomically.  With MC a unit
-  // is a pair of M tiles (2p, 2p+1): CTA rank r of the cluster takes tile 2p+r
-  // (rows past M, when mt is odd, are loaded as zeros and not stored).
+  // work unit u = (output tile u % ntiles, K slice u / ntiles); slices > 1 only for
+  // the F32 / RESID epilogues, which then add their partial sums atomically
   const int ks = g.ksplit > 1 ? g.ksplit : 1;
-  const int rank = MC ? (int)cluster_ctarank() : 0;
-  const int ustart = MC ? (int)blockIdx.x / 2 : (int)blockIdx.x;
-  const int ustride = MC ? (int)gridDim.x / 2 : (int)gridDim.x;
-  const int mtu = MC ? (mt + 1) / 2 : mt;
-  const int tiles_u = mtu * nt;
-  const int nunits = tiles_u * ks;
-  auto unit = [&](int u, int& mtile, int& ntile, int& sl) {
-    const int t = u % tiles_u;
-    sl = u / tiles_u;
-    mtile = (t % mtu) * (MC ? 2 : 1) + rank;
-    ntile = t / mtu;
-  };
+  const int nunits = ntiles * ks;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], MC ? 2 : 1);  // with MC: this CTA's MMA and the peer's
+      mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -257,7 +239,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
-  if constexpr (MC) cluster_sync();  // the peer's multicast loads and commits target initialised barriers
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   pdl_wait();  // the predecessor kernel's outputs are complete and visible from here on
@@ -270,10 +251,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       bool ok = true;
       uint32_t issued = 0;  // bit s: stage s has a fill in flight or landed
       uint32_t iss_par = 0; // bit s: parity of that fill
-      for (int u = ustart; u < nunits && ok; u += ustride) {
-        int mtile, ntile, sl;
-        unit(u, mtile, ntile, sl);
-        const int m0 = mtile * BM, n0 = ntile * BN;
+      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+        const int t = u % ntiles, sl = u / ntiles;
+        const int m0 = (t % mt) * BM, n0 = (t / mt) * BN;
         const int kb0 = (int)((long)sl * nk / ks), kb1 = (int)((long)(sl + 1) * nk / ks);
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, g.err, DERR_TIMEOUT_PRODUCER)) {
@@ -283,18 +263,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           uint8_t* st = smem + s * C::STAGE;
           mbar_expect_tx(&full[s], C::STAGE);
           load_tile<BM>(st, &tA, &full[s], m0, kb * BK, g.a_mn);
-          if constexpr (MC) {  // this CTA's half of B, into both CTAs
-            uint8_t* bd = st + C::A_BYTES;
-            if (!g.b_mn) {
-              tma_load_2d_mc(bd + rank * (BN / 2) * 128, &tB, &full[s], kb * BK, n0 + rank * (BN / 2), 0x3);
-            } else {
-#pragma unroll
-              for (int j = 0; j < BN / 64; ++j)
-                if ((j & 1) == rank) tma_load_2d_mc(bd + j * (BK * 128), &tB, &full[s], n0 + 64 * j, kb * BK, 0x3);
-            }
-          } else {
-            load_tile<BN>(st + C::A_BYTES, &tB, &full[s], n0, kb * BK, g.b_mn);
-          }
+          load_tile<BN>(st + C::A_BYTES, &tB, &full[s], n0, kb * BK, g.b_mn);
           if (SPLIT) {
             load_tile<BM>(st + C::A_BYTES + C::B_BYTES, &tAl, &full[s], m0, kb * BK, g.a_mn);
             load_tile<BN>(st + 2 * C::A_BYTES + C::B_BYTES, &tBl, &full[s], n0, kb * BK, g.b_mn);
@@ -320,8 +289,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t ph = 0;
     int it = 0;
     bool ok = true;
-    for (int u = ustart; u < nunits && ok; u += ustride, ++it) {
-      const int sl = u / tiles_u;
+    for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++it) {
+      const int sl = u / ntiles;
       const int kb0 = (int)((long)sl * nk / ks), kb1 = (int)((long)(sl + 1) * nk / ks);
       const int buf = it & 1;
       const uint32_t use = (uint32_t)(it >> 1);
@@ -347,8 +316,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mma_bf16_w(dt, dal, db, idesc, 1u);
           }
         }
-        if constexpr (MC) mma_commit_mc_w(&empty[s], 0x3);  // both CTAs may refill the stage
-        else mma_commit_w(&empty[s]);
+        mma_commit_w(&empty[s]);
         if (++s == C::STAGES) {
           s = 0;
           ph ^= 1u;
@@ -364,14 +332,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int half = (warp - 2) >> 2;   // the two warps of a quadrant take alternate column chunks
     const bool exact = g.ol != nullptr; // bf16 remainders are kept: full-precision transcendentals
     int it = 0;
-    for (int u = ustart; u < nunits; u += ustride, ++it) {
-      int mtile, ntile, sl_unused;
-      unit(u, mtile, ntile, sl_unused);
+    for (int u = blockIdx.x; u < nunits; u += gridDim.x, ++it) {
+      const int t = u % ntiles;
       const int buf = it & 1;
       const uint32_t use = (uint32_t)(it >> 1);
       const bool got = mbar_wait(&tfull[buf], use & 1u, abort_flag, g.err, DERR_TIMEOUT_EPILOGUE);
       if (!__all_sync(0xffffffffu, got)) break;  // warp-uniform: tcgen05.ld below is .sync.aligned
       tc_fence_after();
+      const int mtile = t % mt, ntile = t / mt;
       const int row = mtile * BM + q * 32 + lane;
       const int n0 = ntile * BN;
       const bool rok = row < g.M;
@@ -613,7 +581,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if constexpr (MC) cluster_sync();  // no multicast into, or commit onto, this CTA after it exits
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
@@ -627,11 +594,11 @@ bool operand_map(CUtensorMap* m, const bf16* p, const Opnd& o, int rows, int K, 
   return make_map(m, p, (uint64_t)rows, (uint64_t)K, (uint64_t)o.ld, 64u);
 }
 
-template <int BN, bool SPLIT, int EPI, int DH = 0, bool MC = false>
+template <int BN, bool SPLIT, int EPI, int DH = 0>
 int launch(const CUtensorMap& a, const CUtensorMap& al, const CUtensorMap& b, const CUtensorMap& bl,
            const GemmArgs& g, cudaStream_t st) {
   using C = Cfg<BN, SPLIT>;
-  auto kern = gemm_kernel<BN, SPLIT, EPI, DH, MC>;
+  auto kern = gemm_kernel<BN, SPLIT, EPI, DH>;
   constexpr bool kCo = EPI == EPI_F32 || EPI == EPI_OPND || EPI == EPI_RESID || EPI == EPI_GELU ||
                       EPI == EPI_GELU_BWD || EPI == EPI_SGD;
   constexpr int SMEM = C::SMEM + (kCo ? kXposeBytes : 0);
@@ -642,35 +609,26 @@ int launch(const CUtensorMap& a, const CUtensorMap& al, const CUtensorMap& b, co
     if (e != cudaSuccess) return (int)e;
     attr_set = true;
   }
-  const int ks = g.ksplit > 1 ? g.ksplit : 1;
-  if constexpr (MC) {  // clusters of two CTAs, one per pair of M tiles
-    const int units = ((g.M + 2 * BM - 1) / (2 * BM)) * ((g.N + BN - 1) / BN) * ks;
-    const int clusters = units < num_sms() / 2 ? units : num_sms() / 2;
-    return (int)launch_k_cluster(kern, dim3(2 * clusters), dim3(kGemmThreads), SMEM, st, 2u, a, al, b, bl, g);
-  }
-  const int tiles = ((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN) * ks;
+  const int tiles = ((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN) * (g.ksplit > 1 ? g.ksplit : 1);
   const int grid = tiles < num_sms() ? tiles : num_sms();
   return (int)launch_k(kern, dim3(grid), dim3(kGemmThreads), SMEM, st, a, al, b, bl, g);
 }
 
-template <int BN, bool SPLIT, bool MC = false>
+template <int BN, bool SPLIT>
 int dispatch_epi(int epi, const CUtensorMap& a, const CUtensorMap& al, const CUtensorMap& b,
                  const CUtensorMap& bl, const GemmArgs& g, cudaStream_t st) {
   switch (epi) {
-    case EPI_F32: return launch<BN, SPLIT, EPI_F32, 0, MC>(a, al, b, bl, g, st);
-    case EPI_OPND: return launch<BN, SPLIT, EPI_OPND, 0, MC>(a, al, b, bl, g, st);
-    case EPI_RESID: return launch<BN, SPLIT, EPI_RESID, 0, MC>(a, al, b, bl, g, st);
-    case EPI_GELU: return launch<BN, SPLIT, EPI_GELU, 0, MC>(a, al, b, bl, g, st);
-    case EPI_GELU_BWD: return launch<BN, SPLIT, EPI_GELU_BWD, 0, MC>(a, al, b, bl, g, st);
-    case EPI_SGD: return launch<BN, SPLIT, EPI_SGD, 0, MC>(a, al, b, bl, g, st);
-    case EPI_CE_FWD: return launch<BN, SPLIT, EPI_CE_FWD, 0, MC>(a, al, b, bl, g, st);
-    case EPI_CE_BWD: return launch<BN, SPLIT, EPI_CE_BWD, 0, MC>(a, al, b, bl, g, st);
+    case EPI_F32: return launch<BN, SPLIT, EPI_F32>(a, al, b, bl, g, st);
+    case EPI_OPND: return launch<BN, SPLIT, EPI_OPND>(a, al, b, bl, g, st);
+    case EPI_RESID: return launch<BN, SPLIT, EPI_RESID>(a, al, b, bl, g, st);
+    case EPI_GELU: return launch<BN, SPLIT, EPI_GELU>(a, al, b, bl, g, st);
+    case EPI_GELU_BWD: return launch<BN, SPLIT, EPI_GELU_BWD>(a, al, b, bl, g, st);
+    case EPI_SGD: return launch<BN, SPLIT, EPI_SGD>(a, al, b, bl, g, st);
+    case EPI_CE_FWD: return launch<BN, SPLIT, EPI_CE_FWD>(a, al, b, bl, g, st);
+    case EPI_CE_BWD: return launch<BN, SPLIT, EPI_CE_BWD>(a, al, b, bl, g, st);
   }
   return (int)cudaErrorInvalidValue;
 }
-
-// Paired CTAs sharing B through multicast: bf16 operands, a wide tile, at least two M tiles.
-bool use_pairs(int M, int bn, bool split) { return !split && bn >= 192 && M > BM; }
 
 }  // namespace
 
@@ -715,14 +673,6 @@ int qkv_rope_bn(int dh, int d, bool split) {
 template <bool SPLIT>
 int launch_qkv_rope(int bn, int dh, const CUtensorMap& a, const CUtensorMap& al, const CUtensorMap& b,
                     const CUtensorMap& bl, const GemmArgs& g, cudaStream_t st) {
-  if constexpr (!SPLIT) {
-    if (use_pairs(g.M, bn, false)) {
-      if (bn == 192 && dh == 96) return launch<192, false, EPI_QKV_ROPE, 96, true>(a, al, b, bl, g, st);
-      if (bn == 256 && dh == 64) return launch<256, false, EPI_QKV_ROPE, 64, true>(a, al, b, bl, g, st);
-      if (bn == 256 && dh == 128) return launch<256, false, EPI_QKV_ROPE, 128, true>(a, al, b, bl, g, st);
-      if (bn == 256 && dh == 32) return launch<256, false, EPI_QKV_ROPE, 32, true>(a, al, b, bl, g, st);
-    }
-  }
   if (bn == 256 && dh == 32) return launch<256, SPLIT, EPI_QKV_ROPE, 32>(a, al, b, bl, g, st);
   if (bn == 256 && dh == 64) return launch<256, SPLIT, EPI_QKV_ROPE, 64>(a, al, b, bl, g, st);
   if (bn == 128 && dh == 32) return launch<128, SPLIT, EPI_QKV_ROPE, 32>(a, al, b, bl, g, st);
@@ -744,8 +694,7 @@ int gemm_qkv_rope(const Opnd& A, const Opnd& B, GemmArgs g, int dh, bool split, 
   g.a_mn = A.mn;
   g.b_mn = B.mn;
   CUtensorMap a, al, b, bl;
-  const int bbox = use_pairs(g.M, bn, split) && !B.mn ? bn / 2 : bn;  // paired CTAs load half of B each
-  if (!operand_map(&a, A.hi, A, g.M, g.K, BM) || !operand_map(&b, B.hi, B, g.N, g.K, bbox))
+  if (!operand_map(&a, A.hi, A, g.M, g.K, BM) || !operand_map(&b, B.hi, B, g.N, g.K, bn))
     return (int)cudaErrorInvalidValue;
   al = a;
   bl = b;
@@ -802,16 +751,12 @@ int gemm_run(int epi, const Opnd& A, const Opnd& B, GemmArgs g, bool split, cuda
     if (e != cudaSuccess) return (int)e;
   }
   CUtensorMap a, al, b, bl;
-  const bool mc = use_pairs(g.M, bn, split);
-  const int bbox = mc && !B.mn ? bn / 2 : bn;  // paired CTAs load half of B each
-  if (!operand_map(&a, A.hi, A, g.M, g.K, BM) || !operand_map(&b, B.hi, B, g.N, g.K, bbox))
+  if (!operand_map(&a, A.hi, A, g.M, g.K, BM) || !operand_map(&b, B.hi, B, g.N, g.K, bn))
     return (int)cudaErrorInvalidValue;
   al = a;
   bl = b;
   if (split && (!operand_map(&al, A.lo, A, g.M, g.K, BM) || !operand_map(&bl, B.lo, B, g.N, g.K, bn)))
     return (int)cudaErrorInvalidValue;
-  if (mc) return bn == 192 ? dispatch_epi<192, false, true>(epi, a, al, b, bl, g, st)
-                           : dispatch_epi<256, false, true>(epi, a, al, b, bl, g, st);
   if (bn == 128)
     return split ? dispatch_epi<128, true>(epi, a, al, b, bl, g, st) : dispatch_epi<128, false>(epi, a, al, b, bl, g, st);
   if (bn == 192)

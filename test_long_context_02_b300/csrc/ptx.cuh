@@ -117,28 +117,6 @@ TTT_DEV void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x
       : "memory");
 }
 
-// ------------------------------------------------------------ thread-block clusters
-// Rank of this CTA in its cluster.
-TTT_DEV uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// Every thread of every CTA of the cluster arrives, then waits for all of them.
-TTT_DEV void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// 2-D tiled TMA load written to the same shared-memory offset in every CTA of
-// the cluster named by cta_mask; each destination CTA's mbarrier at the offset
-// of `bar` receives the bytes that land in it.
-TTT_DEV void tma_load_2d_mc(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(cta_mask)
-      : "memory");
-}
-
 // ----------------------------------------------------------------- tcgen05
 TTT_DEV void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {  // whole warp
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
@@ -321,17 +299,6 @@ TTT_DEV void mma_bf16_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uin
       "elect.sync _|e, 0xffffffff;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// Whole-warp form: once every tcgen05.mma issued so far by this thread completes,
-// arrive once on the mbarrier at the offset of `bar` in each CTA of cta_mask.
-TTT_DEV void mma_commit_mc_w(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "{\n\t.reg .pred e;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(
-          smem_u32(bar)),
-      "h"(cta_mask)
       : "memory");
 }
 TTT_DEV void mma_commit_w(uint64_t* bar) {

@@ -75,13 +75,11 @@ def test_gemm_f32_layouts(M, N, K, a_mn, b_mn):
     assert rel(got, ref) < 2e-6, (M, N, K, a_mn, b_mn)
 
 
-# Shapes whose tile choice is 256 or 192 wide with at least two M tiles: the kernel then runs
-# as clusters of two CTAs on adjacent M tiles that share each B tile (each loads half of it
-# and multicasts it to both).  1152 rows give an odd tile count, so the second CTA of the
-# last pair computes a tile that lies wholly past M.
+# Shapes of the benchmark's size class, where the tile choice is 256 or 192 wide and each
+# persistent CTA takes several tiles (1152 rows: an odd number of row tiles).
 @pytest.mark.parametrize("M,N,K", [(1152, 4096, 320), (1024, 6144, 256), (2048, 1536, 1024)])
 @pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 0), (1, 1)])
-def test_gemm_paired_ctas(M, N, K, a_mn, b_mn):
+def test_gemm_wide_tiles(M, N, K, a_mn, b_mn):
     a, b, Aq, Bq = operands(M, N, K, a_mn, b_mn)
     out = torch.full((M, N), float("nan"), dtype=torch.float32, device=dev)
     err = errword()
