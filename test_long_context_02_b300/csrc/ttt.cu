@@ -84,6 +84,10 @@ struct ttt_ctx {
   Pair sxn;                             // [b][d] normalised attention input of the trainable blocks
   cudaStream_t st2 = nullptr;           // the frozen-prefix passes run ahead on this stream
   cudaEvent_t ev_fork = nullptr, ev_pass[2] = {nullptr, nullptr}, ev_suf[2] = {nullptr, nullptr};
+  // the fast-weight gradient products with their SGD step run on a third stream beside
+  // the rest of the chunk's backward (nothing in it reads the updated weights)
+  cudaStream_t st3 = nullptr;
+  cudaEvent_t ev_da = nullptr, ev_dx = nullptr, ev_wd = nullptr, ev_wu = nullptr;
   Pair kown, vown;           // [L][R][d]
   float *sx = nullptr, *sh = nullptr, *srs_a = nullptr, *srs_m = nullptr, *slse = nullptr, *sa = nullptr;
   Pair sq, so, sxm, su;
@@ -447,9 +451,20 @@ int suffix_step(ttt_ctx* c, int s, int row, const int* tok, int n, const int* ne
   RUN(K_RMSNORM, 1, 0, 0, nn * dd * (12 + eb),
       rows_rmsnorm_bwd(c->dxn, c->x, c->gains + (long)(2 * L) * d, c->rs_f, nullptr, n, d, c->dy, c->dy16.hi,
                        c->dy16.lo, st));
+  // The dW + SGD products go to the third stream when it is free to run beside the rest:
+  //   W_down step after dA (which reads W_down and dY)      -> before dY is overwritten
+  //   W_up step after dXn (which reads W_up) and dA        -> before dA is overwritten
+  //   all steps done before the chunk ends (the next chunk's forward reads the weights).
+  const bool side = c->st3 != nullptr && c->prof_mask == 0;
+  cudaStream_t sw = side ? c->st3 : st;
+  bool wd_pending = false, wu_pending = false;
   for (int si = S - 1; si >= 0; --si) {
     const int l = P0 + si;
     Pair up16 = sq_.up16.at((long)si * d * f), down16 = sq_.down16.at((long)si * f * d);
+    if (wu_pending) {  // the previous block's W_up step has read dA
+      CK(cudaStreamWaitEvent(st, c->ev_wu, 0));
+      wu_pending = false;
+    }
     {  // dA = (dY W_down^T) * gelu'(a)
       GemmArgs g;
       g.M = n; g.N = f; g.K = d;
@@ -459,12 +474,20 @@ int suffix_step(ttt_ctx* c, int s, int row, const int* tok, int n, const int* ne
           gemm_run(EPI_GELU_BWD, opnd(c->dy16, d, 0), opnd(down16, d, 0), g, sp, st));
     }
     {  // W_down -= eta U^T dY
+      if (side) {
+        CK(cudaEventRecord(c->ev_da, st));
+        CK(cudaStreamWaitEvent(sw, c->ev_da, 0));
+      }
       GemmArgs g;
       g.M = f; g.N = d; g.K = n;
       g.w32 = sq_.down32 + (long)si * f * d; g.wh = down16.hi; g.wl = down16.lo; g.ldw = d; g.eta = eta;
       g.err = c->derr;
       RUN(K_DW_SGD, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 8 * dd * ff,
-          gemm_run(EPI_SGD, opnd(c->su.at((long)si * b * f), f, 1), opnd(c->dy16, d, 1), g, sp, st));
+          gemm_run(EPI_SGD, opnd(c->su.at((long)si * b * f), f, 1), opnd(c->dy16, d, 1), g, sp, sw));
+      if (side) {
+        CK(cudaEventRecord(c->ev_wd, sw));
+        wd_pending = true;
+      }
     }
     if (si > 0) {  // dXn_m = dA W_up^T  (before W_up changes)
       GemmArgs g;
@@ -487,12 +510,20 @@ int suffix_step(ttt_ctx* c, int s, int row, const int* tok, int n, const int* ne
           gemm_run(EPI_RESID, opnd(c->da_s, f, 0), opnd(c->Wup_s.at((long)si * d * f), f, 0), g2, sp, st));
     }
     {  // W_up -= eta Xn_m^T dA
+      if (side) {
+        CK(cudaEventRecord(c->ev_dx, st));
+        CK(cudaStreamWaitEvent(sw, c->ev_dx, 0));
+      }
       GemmArgs g;
       g.M = d; g.N = f; g.K = n;
       g.w32 = sq_.up32 + (long)si * d * f; g.wh = up16.hi; g.wl = up16.lo; g.ldw = f; g.eta = eta;
       g.err = c->derr;
       RUN(K_DW_SGD, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 8 * dd * ff,
-          gemm_run(EPI_SGD, opnd(c->sxm.at((long)si * b * d), d, 1), opnd(c->da, f, 1), g, sp, st));
+          gemm_run(EPI_SGD, opnd(c->sxm.at((long)si * b * d), d, 1), opnd(c->da, f, 1), g, sp, sw));
+      if (side) {
+        CK(cudaEventRecord(c->ev_wu, sw));
+        wu_pending = true;
+      }
     }
     if (si == 0) break;  // the first trainable block's attention needs no gradient
     // dH = dY + RMSNorm_m^T(dXn_m)
@@ -545,10 +576,18 @@ int suffix_step(ttt_ctx* c, int s, int row, const int* tok, int n, const int* ne
       RUN(K_ATTN_DX, 1, 6 * nn * dd * dd, 6 * nn * dd * dd * ops, 0,
           gemm_run(EPI_F32, opnd(c->dqkv, 3 * d, 0), opnd(c->Wqkv.at((long)l * d * 3 * d), 3 * d, 0), g, sp, st));
     }
+    if (wd_pending) {  // the W_down step has read dY
+      CK(cudaStreamWaitEvent(st, c->ev_wd, 0));
+      wd_pending = false;
+    }
     // dY_{l-1} = dH + RMSNorm_a^T(dXn_a)
     RUN(K_RMSNORM, 1, 0, 0, nn * dd * (20 + eb),
         rows_rmsnorm_bwd(c->dxn, c->sx + (long)si * b * d, c->gains + (long)(2 * l) * d, c->srs_a + (long)si * b,
                          c->dh32, n, d, c->dy, c->dy16.hi, c->dy16.lo, st));
+  }
+  if (side) {  // every step of this chunk is in place before anything later reads the weights
+    CK(cudaStreamWaitEvent(st, c->ev_wd, 0));
+    CK(cudaStreamWaitEvent(st, c->ev_wu, 0));
   }
   // ------------------------------------------------------------------- commit
   const double cb = (double)S * nn * dd * 2 * 2;
@@ -685,6 +724,11 @@ extern "C" int ttt_create(const ttt_config* cfg, void* cuda_stream, ttt_ctx** ou
     return TTT_ERR_OOM;
   }
   if (cudaStreamCreateWithFlags(&c->st2, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&c->st3, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&c->ev_da, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&c->ev_dx, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&c->ev_wd, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&c->ev_wu, cudaEventDisableTiming) != cudaSuccess ||
       cudaEventCreateWithFlags(&c->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
       cudaEventCreateWithFlags(&c->ev_pass[0], cudaEventDisableTiming) != cudaSuccess ||
       cudaEventCreateWithFlags(&c->ev_pass[1], cudaEventDisableTiming) != cudaSuccess ||
@@ -711,9 +755,12 @@ extern "C" void ttt_destroy(ttt_ctx* c) {
   if (!c) return;
   if (c->st) cudaStreamSynchronize(c->st);
   if (c->st2) cudaStreamSynchronize(c->st2);
+  if (c->st3) cudaStreamSynchronize(c->st3);
   cudaDeviceSynchronize();
   if (c->st2) cudaStreamDestroy(c->st2);
-  for (cudaEvent_t e : {c->ev_fork, c->ev_pass[0], c->ev_pass[1], c->ev_suf[0], c->ev_suf[1]})
+  if (c->st3) cudaStreamDestroy(c->st3);
+  for (cudaEvent_t e : {c->ev_fork, c->ev_pass[0], c->ev_pass[1], c->ev_suf[0], c->ev_suf[1], c->ev_da, c->ev_dx,
+                        c->ev_wd, c->ev_wu})
     if (e) cudaEventDestroy(e);
   for (void* p : c->allocs) cudaFree(p);
   if (c->seq_tok) cudaFree(c->seq_tok);
