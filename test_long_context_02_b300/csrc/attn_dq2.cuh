@@ -32,8 +32,9 @@ struct Q2Cfg {
   static constexpr int NOP = SPLIT ? 2 : 1;
   static constexpr int Q_OFF = 0;
   static constexpr int DO_OFF = NOP * TILE;
-  static constexpr int K_OFF = 2 * NOP * TILE;          // 2 stages
-  static constexpr int V_OFF = K_OFF + 2 * NOP * TILE;  // 2 stages
+  static constexpr int KST = 3;                         // key stages
+  static constexpr int K_OFF = 2 * NOP * TILE;
+  static constexpr int V_OFF = K_OFF + KST * NOP * TILE;  // 2 stages
   static constexpr int BAR_OFF = V_OFF + 2 * NOP * TILE;
   static constexpr int SMEM = BAR_OFF + 256;
   static_assert(SMEM <= 232448, "dQ kernel exceeds shared memory");
@@ -109,15 +110,15 @@ TTT_DEV void dq2_body(const CUtensorMap* tQ, const CUtensorMap* tQl, const CUten
   }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
   uint64_t* q_full = bars;        // 1 (Q and dO)
-  uint64_t* k_full = bars + 1;    // 2
-  uint64_t* k_empty = bars + 3;   // 2
-  uint64_t* v_full = bars + 5;    // 2
-  uint64_t* v_empty = bars + 7;   // 2
-  uint64_t* s_full = bars + 9;    // 2 (per score buffer: S_j and dP_j landed)
-  uint64_t* ds_full = bars + 11;  // 2 (per score buffer)
-  uint64_t* dq_full = bars + 13;  // 1
-  uint64_t* drain = bars + 14;    // 1
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
+  uint64_t* k_full = bars + 1;    // 3
+  uint64_t* k_empty = bars + 4;   // 3
+  uint64_t* v_full = bars + 7;    // 2
+  uint64_t* v_empty = bars + 9;   // 2
+  uint64_t* s_full = bars + 11;   // 2 (per score buffer: S_j and dP_j landed)
+  uint64_t* ds_full = bars + 13;  // 2 (per score buffer)
+  uint64_t* dq_full = bars + 15;  // 1
+  uint64_t* drain = bars + 16;    // 1
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const AttnArgs& g = a.g;
@@ -128,9 +129,11 @@ TTT_DEV void dq2_body(const CUtensorMap* tQ, const CUtensorMap* tQl, const CUten
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::KST; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
@@ -173,15 +176,17 @@ TTT_DEV void dq2_body(const CUtensorMap* tQ, const CUtensorMap* tQl, const CUten
       for (int j = 0; j < J; ++j) {
         const int s = j & 1;
         const uint32_t par = (uint32_t)((j >> 1) & 1);
+        const int ks = j % C::KST;
+        const uint32_t kp = (uint32_t)((j / C::KST) & 1);
         bool own;
         const int row0 = tile_row0(j, own);
-        if (!mbar_wait(&k_empty[s], par ^ 1u, abort_flag, g.err, DERR_TIMEOUT_PRODUCER)) break;
-        uint8_t* kd = smem + C::K_OFF + s * C::NOP * C::TILE;
-        mbar_expect_tx(&k_full[s], C::NOP * C::TILE);
-        load_tile_q2<C::NATOM>(kd, own ? tKo : tKr, &k_full[s], col0, row0);
-        if (SPLIT) load_tile_q2<C::NATOM>(kd + C::TILE, own ? tKol : tKrl, &k_full[s], col0, row0);
-        kiss |= 1u << s;
-        kpar = (kpar & ~(1u << s)) | (par << s);
+        if (!mbar_wait(&k_empty[ks], kp ^ 1u, abort_flag, g.err, DERR_TIMEOUT_PRODUCER)) break;
+        uint8_t* kd = smem + C::K_OFF + ks * C::NOP * C::TILE;
+        mbar_expect_tx(&k_full[ks], C::NOP * C::TILE);
+        load_tile_q2<C::NATOM>(kd, own ? tKo : tKr, &k_full[ks], col0, row0);
+        if (SPLIT) load_tile_q2<C::NATOM>(kd + C::TILE, own ? tKol : tKrl, &k_full[ks], col0, row0);
+        kiss |= 1u << ks;
+        kpar = (kpar & ~(1u << ks)) | (kp << ks);
         if (!mbar_wait(&v_empty[s], par ^ 1u, abort_flag, g.err, DERR_TIMEOUT_PRODUCER)) break;
         uint8_t* vd = smem + C::V_OFF + s * C::NOP * C::TILE;
         mbar_expect_tx(&v_full[s], C::NOP * C::TILE);
@@ -191,10 +196,10 @@ TTT_DEV void dq2_body(const CUtensorMap* tQ, const CUtensorMap* tQl, const CUten
         vpar = (vpar & ~(1u << s)) | (par << s);
       }
       drain_q2(q_full, 0, g.err);
-      for (int s = 0; s < 2; ++s) {
+      for (int s = 0; s < C::KST; ++s)
         if (kiss & (1u << s)) drain_q2(&k_full[s], (kpar >> s) & 1u, g.err);
+      for (int s = 0; s < 2; ++s)
         if (viss & (1u << s)) drain_q2(&v_full[s], (vpar >> s) & 1u, g.err);
-      }
     }
   } else if (warp == 1) {  // MMA issuer: the whole warp, one elected lane issues
     auto wait_all = [&](uint64_t* bar, uint32_t par) -> bool {
@@ -213,31 +218,12 @@ TTT_DEV void dq2_body(const CUtensorMap* tQ, const CUtensorMap* tQl, const CUten
         }
       }
     };
-    bool ok = J > 0 && wait_all(q_full, 0) &&
-              wait_all(&k_full[0], 0);
-    if (ok) {
-      tc_fence_after();
-      xk(tmem, qb, smem_u32(smem + C::K_OFF));  // S_0
-    }
-    for (int j = 0; j < J && ok; ++j) {
-      const int s = j & 1;
-      if (!wait_all(&v_full[s], (uint32_t)((j >> 1) & 1))) break;
-      tc_fence_after();
-      // dP_j = dO V_j^T (the softmax finished reading dP_{j-1} before dS_{j-1} was signalled)
-      xk(tmem + T_DP, dob, smem_u32(smem + C::V_OFF + s * C::NOP * C::TILE));
-      mma_commit_w(&s_full[s]);
-      mma_commit_w(&v_empty[s]);
-      if (j + 1 < J) {  // S_{j+1} into the other buffer: its dS_{j-1} K_{j-1} product was issued last round
-        if (!wait_all(&k_full[s ^ 1], (uint32_t)(((j + 1) >> 1) & 1))) break;
-        tc_fence_after();
-        xk(tmem + (uint32_t)((s ^ 1) * 128), qb, smem_u32(smem + C::K_OFF + (s ^ 1) * C::NOP * C::TILE));
-      }
-      if (!wait_all(&ds_full[s], (uint32_t)((j >> 1) & 1))) break;
-      tc_fence_after();
-      // dQ += dS_j K_j; dS_j: keys 0-63 in columns [0,32) (+ remainders [32,64)), keys 64-127 in
-      // [64,96) (+ [96,128)) of score buffer s
-      const uint32_t kb = smem_u32(smem + C::K_OFF + s * C::NOP * C::TILE);
-      const uint32_t pb = tmem + (uint32_t)(s * 128);
+    auto kstage = [&](int j) { return smem_u32(smem + C::K_OFF + (j % C::KST) * C::NOP * C::TILE); };
+    // dQ += dS_j K_j; dS_j: keys 0-63 in columns [0,32) (+ remainders [32,64)), keys 64-127 in
+    // [64,96) (+ [96,128)) of score buffer j & 1
+    auto dq_mma = [&](int j) {
+      const uint32_t kb = kstage(j);
+      const uint32_t pb = tmem + (uint32_t)((j & 1) * 128);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const uint32_t pa = pb + (uint32_t)((kk < 4 ? 0 : 64) + 8 * (kk & 3));
@@ -247,7 +233,46 @@ TTT_DEV void dq2_body(const CUtensorMap* tQ, const CUtensorMap* tQl, const CUten
           mma_bf16_ts_w(tmem + T_DQ, pa + 32u, mndesc_q2(kb, kk), idDQ, 1u);
         }
       }
-      mma_commit_w(&k_empty[s]);
+      mma_commit_w(&k_empty[j % C::KST]);
+    };
+    // Tensor-pipe order per key tile j: dP_j, dQ_{j-1}, S_{j+1}.  The softmax of tile j needs
+    // only S_j (issued a tile earlier) and dP_j, so it runs while dQ_{j-1} and S_{j+1}
+    // execute.  S_{j+1} overwrites the score buffer of dS_{j-1}, after dQ_{j-1} in issue
+    // order; K_{j+1} has a stage of its own (three key stages), so its load does not wait
+    // for dQ_{j-1} to release K_{j-1}.
+    bool ok = J > 0 && wait_all(q_full, 0) && wait_all(&k_full[0], 0);
+    if (ok) {
+      tc_fence_after();
+      xk(tmem, qb, kstage(0));  // S_0
+    }
+    for (int j = 0; j < J && ok; ++j) {
+      const int s = j & 1;
+      if (!wait_all(&v_full[s], (uint32_t)((j >> 1) & 1))) {
+        ok = false;
+        break;
+      }
+      // the softmax of tile j-1 has read dP_{j-1} and written dS_{j-1}
+      if (j > 0 && !wait_all(&ds_full[s ^ 1], (uint32_t)(((j - 1) >> 1) & 1))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      xk(tmem + T_DP, dob, smem_u32(smem + C::V_OFF + s * C::NOP * C::TILE));  // dP_j = dO V_j^T
+      mma_commit_w(&s_full[s]);
+      mma_commit_w(&v_empty[s]);
+      if (j > 0) dq_mma(j - 1);
+      if (j + 1 < J) {  // S_{j+1} into the other score buffer
+        if (!wait_all(&k_full[(j + 1) % C::KST], (uint32_t)(((j + 1) / C::KST) & 1))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        xk(tmem + (uint32_t)((s ^ 1) * 128), qb, kstage(j + 1));
+      }
+    }
+    if (ok && wait_all(&ds_full[(J - 1) & 1], (uint32_t)(((J - 1) >> 1) & 1))) {
+      tc_fence_after();
+      dq_mma(J - 1);
     }
     mma_commit_w(dq_full);
     mma_commit_w(drain);
