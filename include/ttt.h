@@ -220,6 +220,18 @@ TTT_API int ttt_import_state(ttt_ctx* ctx, int32_t seq, const void* host_buf, si
  */
 TTT_API int ttt_reset(ttt_ctx* ctx);
 
+/*
+ * on = 1 (the default): within a sequence, the frozen-block pass of the next
+ * group of chunks runs on a second stream of the context beside the current
+ * group's trainable steps, and the fast-weight gradient products with their SGD
+ * step run on a third stream beside the rest of each chunk's backward.
+ * on = 0: every kernel runs on the context stream in issue order (per-kernel
+ * timings then measure each kernel alone).  Results are the same either way,
+ * up to the summation order of K-sliced products.  Synchronises the context
+ * stream; returns TTT_ERR_ARG for another value.
+ */
+TTT_API int ttt_set_concurrency(ttt_ctx* ctx, int32_t on);
+
 /* Kernels launched by this context since it was created (monotonic counter). */
 TTT_API int64_t ttt_launch_count(const ttt_ctx* ctx);
 

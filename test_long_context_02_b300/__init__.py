@@ -132,6 +132,7 @@ ttt_last_error = _sig("ttt_last_error", ctypes.c_char_p, _vp)
 ttt_reset = _sig("ttt_reset", ctypes.c_int, _vp)
 ttt_get_window = _sig("ttt_get_window", ctypes.c_int, _vp, _i32, _i32, _vp, _vp, _vp)
 ttt_launch_count = _sig("ttt_launch_count", _i64, _vp)
+ttt_set_concurrency = _sig("ttt_set_concurrency", ctypes.c_int, _vp, _i32)
 ttt_state_bytes = _sig("ttt_state_bytes", _i64, _vp)
 ttt_export_state = _sig("ttt_export_state", ctypes.c_int, _vp, _i32, _vp, ctypes.c_size_t)
 ttt_import_state = _sig("ttt_import_state", ctypes.c_int, _vp, _i32, _vp, ctypes.c_size_t)
@@ -299,6 +300,10 @@ class TTT:
     def import_state(self, state: bytes, seq: int = 0):
         buf = np.frombuffer(state, np.uint8)
         self._check(ttt_import_state(self._h, seq, buf.ctypes.data, buf.size), "ttt_import_state")
+
+    def set_concurrency(self, on: bool):
+        """Second/third-stream overlap inside the context (on by default); off runs in issue order."""
+        self._check(ttt_set_concurrency(self._h, 1 if on else 0), "ttt_set_concurrency")
 
     def reset(self):
         self._check(ttt_reset(self._h), "ttt_reset")

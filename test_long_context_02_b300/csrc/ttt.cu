@@ -88,6 +88,7 @@ struct ttt_ctx {
   // the rest of the chunk's backward (nothing in it reads the updated weights)
   cudaStream_t st3 = nullptr;
   cudaEvent_t ev_da = nullptr, ev_dx = nullptr, ev_wd = nullptr, ev_wu = nullptr;
+  bool concurrent = true;  // use the second and third streams (ttt_set_concurrency)
   Pair kown, vown;           // [L][R][d]
   float *sx = nullptr, *sh = nullptr, *srs_a = nullptr, *srs_m = nullptr, *slse = nullptr, *sa = nullptr;
   Pair sq, so, sxm, su;
@@ -210,16 +211,17 @@ cudaEvent_t next_event(ttt_ctx* c) {
   return c->ev_pool[c->ev_used++];
 }
 
-// Run one launch site: count its kernels and, when profiling, bracket it with events.
+// Run one launch site: count its kernels and, when profiling, bracket it with events
+// recorded on the stream the site launches on.
 template <class F>
-int site(ttt_ctx* c, int cls, int nkern, double alg, double exec, double bytes, F&& f) {
+int site(ttt_ctx* c, int cls, cudaStream_t sst, int nkern, double alg, double exec, double bytes, F&& f) {
   cudaEvent_t a = nullptr;
-  if (((c->prof_mask >> cls) & 1u) && (a = next_event(c))) cudaEventRecord(a, c->st);
+  if (((c->prof_mask >> cls) & 1u) && (a = next_event(c))) cudaEventRecord(a, sst);
   const int r = f();
   if (a) {
     cudaEvent_t b = next_event(c);
     if (b) {
-      cudaEventRecord(b, c->st);
+      cudaEventRecord(b, sst);
       c->recs.push_back(ProfRec{cls, a, b, alg, exec, bytes, nkern});
     }
   }
@@ -227,7 +229,10 @@ int site(ttt_ctx* c, int cls, int nkern, double alg, double exec, double bytes, 
   return r;
 }
 
-#define RUN(cls, nk, alg, exec, bytes, expr) CK(site(c, cls, nk, alg, exec, bytes, [&]() { return (int)(expr); }))
+// RUN launches on the stream `st` of the enclosing scope; RUN_ON names the stream.
+#define RUN_ON(sst, cls, nk, alg, exec, bytes, expr) \
+  CK(site(c, cls, sst, nk, alg, exec, bytes, [&]() { return (int)(expr); }))
+#define RUN(cls, nk, alg, exec, bytes, expr) RUN_ON(st, cls, nk, alg, exec, bytes, expr)
 
 // Tiles of 128 keys visited by the attention kernels for query tile qt (as the kernels enumerate them).
 long attn_tiles(long pos0, int n, int k, int qt) {
@@ -455,7 +460,7 @@ int suffix_step(ttt_ctx* c, int s, int row, const int* tok, int n, const int* ne
   //   W_down step after dA (which reads W_down and dY)      -> before dY is overwritten
   //   W_up step after dXn (which reads W_up) and dA        -> before dA is overwritten
   //   all steps done before the chunk ends (the next chunk's forward reads the weights).
-  const bool side = c->st3 != nullptr && c->prof_mask == 0;
+  const bool side = c->st3 != nullptr && c->concurrent;
   cudaStream_t sw = side ? c->st3 : st;
   bool wd_pending = false, wu_pending = false;
   for (int si = S - 1; si >= 0; --si) {
@@ -482,8 +487,8 @@ int suffix_step(ttt_ctx* c, int s, int row, const int* tok, int n, const int* ne
       g.M = f; g.N = d; g.K = n;
       g.w32 = sq_.down32 + (long)si * f * d; g.wh = down16.hi; g.wl = down16.lo; g.ldw = d; g.eta = eta;
       g.err = c->derr;
-      RUN(K_DW_SGD, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 8 * dd * ff,
-          gemm_run(EPI_SGD, opnd(c->su.at((long)si * b * f), f, 1), opnd(c->dy16, d, 1), g, sp, sw));
+      RUN_ON(sw, K_DW_SGD, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 8 * dd * ff,
+             gemm_run(EPI_SGD, opnd(c->su.at((long)si * b * f), f, 1), opnd(c->dy16, d, 1), g, sp, sw));
       if (side) {
         CK(cudaEventRecord(c->ev_wd, sw));
         wd_pending = true;
@@ -518,8 +523,8 @@ int suffix_step(ttt_ctx* c, int s, int row, const int* tok, int n, const int* ne
       g.M = d; g.N = f; g.K = n;
       g.w32 = sq_.up32 + (long)si * d * f; g.wh = up16.hi; g.wl = up16.lo; g.ldw = f; g.eta = eta;
       g.err = c->derr;
-      RUN(K_DW_SGD, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 8 * dd * ff,
-          gemm_run(EPI_SGD, opnd(c->sxm.at((long)si * b * d), d, 1), opnd(c->da, f, 1), g, sp, sw));
+      RUN_ON(sw, K_DW_SGD, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 8 * dd * ff,
+             gemm_run(EPI_SGD, opnd(c->sxm.at((long)si * b * d), d, 1), opnd(c->da, f, 1), g, sp, sw));
       if (side) {
         CK(cudaEventRecord(c->ev_wu, sw));
         wu_pending = true;
@@ -939,7 +944,7 @@ int prefill_one(ttt_ctx* c, int s, const int32_t* seq, int T, float* losses) {
     const int t0 = g * G * b, t1 = std::min(T, (g + 1) * G * b);
     return prefix_pass(c, s, seq + t0, t1 - t0, base + t0, st, buf);
   };
-  const bool overlap = ng > 1 && c->prof_mask == 0 && qkv_rope_bn(c->dh, c->d, c->split) != 0;
+  const bool overlap = ng > 1 && c->concurrent && qkv_rope_bn(c->dh, c->d, c->split) != 0;
   if (!overlap) {
     for (int g = 0; g < ng; ++g) {
       int r = pass(g, c->st, 0);
@@ -993,8 +998,8 @@ int logits_row(ttt_ctx* c, const Pair& xf_row, float* z) {
   GemmArgs g;
   g.M = 1; g.N = c->V; g.K = c->d;
   g.out32 = z; g.ldo32 = c->V; g.err = c->derr;
-  RUN(K_CE_FWD, 1, 2 * dd * VV, 2 * dd * VV * (c->split ? 3 : 1), 0,
-      gemm_run(EPI_F32, opnd(xf_row, c->d, 0), opnd(c->Wlm, c->V, 1), g, c->split, c->st));
+  RUN_ON(c->st, K_CE_FWD, 1, 2 * dd * VV, 2 * dd * VV * (c->split ? 3 : 1), 0,
+         gemm_run(EPI_F32, opnd(xf_row, c->d, 0), opnd(c->Wlm, c->V, 1), g, c->split, c->st));
   return TTT_OK;
 }
 }  // namespace
@@ -1237,6 +1242,13 @@ extern "C" int ttt_reset(ttt_ctx* c) {
 }
 
 extern "C" int64_t ttt_launch_count(const ttt_ctx* c) { return c ? c->launches : -1; }
+
+extern "C" int ttt_set_concurrency(ttt_ctx* c, int32_t on) {
+  if (!c || (on != 0 && on != 1)) return TTT_ERR_ARG;
+  if (cudaStreamSynchronize(c->st) != cudaSuccess) return fail(c, TTT_ERR_CUDA, "stream synchronize");
+  c->concurrent = on == 1;
+  return TTT_OK;
+}
 
 extern "C" int ttt_profile(ttt_ctx* c, int64_t class_mask) {
   if (!c) return TTT_ERR_ARG;
