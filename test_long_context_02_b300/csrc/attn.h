@@ -41,6 +41,12 @@ struct AttnBwdArgs {
   const float* D = nullptr;
   float* dq = nullptr; float* dk = nullptr; float* dv = nullptr; long ldg = 0;
   float scale = 0.f;  // 1/sqrt(dh)
+  // Fused output (when qkv_h is set; dq / dk / dv are then not written): the gradient
+  // [dq | dk | dv] with RoPE's rotation transposed on dq and dk, as the bf16 operand
+  // (+ remainder in split mode) of the QKV dX product, row-major [n][ld_qkv]; section
+  // offsets k_off, v_off (columns); angle tables cs / sn [n][dh/2] of the chunk's rows.
+  bf16* qkv_h = nullptr; bf16* qkv_l = nullptr; long ld_qkv = 0, k_off = 0, v_off = 0;
+  const float* cs = nullptr; const float* sn = nullptr;
 };
 struct AttnBwdMaps {
   AttnMaps f;          // q, cache k/v, own k/v as in the forward

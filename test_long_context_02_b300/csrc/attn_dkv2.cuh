@@ -19,6 +19,7 @@
 // dS^T over their own dP^T columns.
 #pragma once
 #include "attn.h"
+#include "attn_bwd_out.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -311,20 +312,32 @@ TTT_DEV void dkv2_body(const CUtensorMap* tQ, const CUtensorMap* tQl, const CUte
       mbar_arrive(ds_full);
     }
     bool got = ok && mbar_wait(acc_full, 0, abort_flag, g.err, DERR_TIMEOUT_EPILOGUE);
-    if (__all_sync(0xffffffffu, got)) {
+    const bool have = __all_sync(0xffffffffu, got);
+    float v[HO], w[HO];
+#pragma unroll
+    for (int e = 0; e < HO; ++e) v[e] = w[e] = 0.f;
+    if (have) {
       tc_fence_after();
-      float v[HO], w[HO];
       ld_cols_k2<HO>(trow + T_DV + hf * HO, v);
       ld_cols_k2<HO>(trow + T_DK + hf * HO, w);
-      if (kvalid) {
-        const float sc = a.scale;
-        float4* dv = reinterpret_cast<float4*>(a.dv + (long)krow * a.ldg + col0 + hf * HO);
-        float4* dk = reinterpret_cast<float4*>(a.dk + (long)krow * a.ldg + col0 + hf * HO);
 #pragma unroll
-        for (int e = 0; e < HO / 4; ++e) {
-          dv[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
-          dk[e] = make_float4(w[4 * e] * sc, w[4 * e + 1] * sc, w[4 * e + 2] * sc, w[4 * e + 3] * sc);
-        }
+      for (int e = 0; e < HO; ++e) w[e] *= a.scale;
+    }
+    if (a.qkv_h) {  // dV as is, dK rotated back; the K, V and Q / dO stages are free now
+      const long o = (long)krow * a.ld_qkv + col0 + hf * HO;
+      if (have && kvalid) store_row_opnd<HO, SPLIT>(a.qkv_h + o + a.v_off, SPLIT ? a.qkv_l + o + a.v_off : nullptr, v);
+      static_assert(rope_bwd_smem_floats<HO>() * 4 <= C::ST_OFF - C::K_OFF, "rope exchange exceeds the stages");
+      const long t0 = 128L * kt;
+      rope_bwd_store<HO, SPLIT>(reinterpret_cast<float*>(smem + C::K_OFF), (warp - 2) * 32 + lane, r, hf, w,
+                                have && kvalid, a.cs + t0 * HO, a.sn + t0 * HO, (int)min(128L, g.n - t0),
+                                a.qkv_h + o + a.k_off, SPLIT ? a.qkv_l + o + a.k_off : nullptr);
+    } else if (have && kvalid) {
+      float4* dv = reinterpret_cast<float4*>(a.dv + (long)krow * a.ldg + col0 + hf * HO);
+      float4* dk = reinterpret_cast<float4*>(a.dk + (long)krow * a.ldg + col0 + hf * HO);
+#pragma unroll
+      for (int e = 0; e < HO / 4; ++e) {
+        dv[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+        dk[e] = make_float4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
       }
     }
   }

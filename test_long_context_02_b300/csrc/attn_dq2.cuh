@@ -15,6 +15,7 @@
 // columns of S_j.
 #pragma once
 #include "attn.h"
+#include "attn_bwd_out.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -335,17 +336,28 @@ TTT_DEV void dq2_body(const CUtensorMap* tQ, const CUtensorMap* tQl, const CUten
       mbar_arrive(&ds_full[s]);
     }
     bool got = ok && mbar_wait(dq_full, 0, abort_flag, g.err, DERR_TIMEOUT_EPILOGUE);
-    if (__all_sync(0xffffffffu, got)) {
-      tc_fence_after();
-      float v[HO];
-      ld_cols_q2<HO>(trow + T_DQ + (uint32_t)(hf * HO), v);
-      if (rvalid) {
-        const float sc = a.scale;
-        float4* dst = reinterpret_cast<float4*>(a.dq + (long)(128 * qt + r) * a.ldg + col0 + hf * HO);
+    const bool have = __all_sync(0xffffffffu, got);
+    float v[HO];
 #pragma unroll
-        for (int e = 0; e < HO / 4; ++e)
-          dst[e] = make_float4(v[4 * e] * sc, v[4 * e + 1] * sc, v[4 * e + 2] * sc, v[4 * e + 3] * sc);
-      }
+    for (int e = 0; e < HO; ++e) v[e] = 0.f;
+    if (have) {
+      tc_fence_after();
+      ld_cols_q2<HO>(trow + T_DQ + (uint32_t)(hf * HO), v);
+#pragma unroll
+      for (int e = 0; e < HO; ++e) v[e] *= a.scale;
+    }
+    const long row = 128L * qt + r;
+    if (a.qkv_h) {  // rotated back and written as the QKV product's operand; the K / V stages are free now
+      static_assert(rope_bwd_smem_floats<HO>() * 4 <= C::BAR_OFF - C::K_OFF, "rope exchange exceeds the stages");
+      const long o = row * a.ld_qkv + col0 + hf * HO;
+      const long t0 = 128L * qt;
+      rope_bwd_store<HO, SPLIT>(reinterpret_cast<float*>(smem + C::K_OFF), (warp - 2) * 32 + lane, r, hf, v,
+                                have && rvalid, a.cs + t0 * HO, a.sn + t0 * HO, (int)min(128L, g.n - t0),
+                                a.qkv_h + o, SPLIT ? a.qkv_l + o : nullptr);
+    } else if (have && rvalid) {
+      float4* dst = reinterpret_cast<float4*>(a.dq + row * a.ldg + col0 + hf * HO);
+#pragma unroll
+      for (int e = 0; e < HO / 4; ++e) dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
     }
   }
   tc_fence_before();

@@ -569,11 +569,12 @@ int suffix_step(ttt_ctx* c, int s, int row, const int* tok, int n, const int* ne
       ba.dv = c->dv;
       ba.ldg = d;
       ba.scale = (float)(1.0 / std::sqrt((double)dh));
+      // written straight into the QKV dX product's operand, RoPE's rotation transposed
+      ba.qkv_h = c->dqkv.hi; ba.qkv_l = c->dqkv.lo; ba.ld_qkv = 3L * d; ba.k_off = d; ba.v_off = 2L * d;
+      ba.cs = cs; ba.sn = sn;
       RUN(K_ATTN_BWD, 1, 4 * dd * (pairs + own_pairs), (6 * dd * tpairs + 8 * dd * own_tile_pairs) * ops, 0,
           attn_bwd_run(m, ba, sp, st, 0));
     }
-    RUN(K_ROPE, 1, 0, 0, nn * dd * (12 + 3 * eb),
-        rows_rope_bwd(c->dq, c->dk, c->dv, cs, sn, n, H, dh, c->dqkv.hi, c->dqkv.lo, st));
     {  // dXn_a = dQKV Wqkv^T
       GemmArgs g;
       g.M = n; g.N = d; g.K = 3 * d;
