@@ -1,8 +1,9 @@
 // Row-wise kernels of the TTT-E2E inner-loop step: token embedding, RMSNorm
-// forward/backward, RoPE (angle table, rotation of q/k with the write of the
-// chunk's own k/v, and its transpose for the backward), the commit of the
-// chunk's keys/values into the k-slot window cache, the cross-entropy
-// combine/mean, and the rowsum(dO * O) term of the attention backward.
+// forward/backward, RoPE (angle table; rotation of q/k with the write of the
+// chunk's own k/v where the QKV product's epilogue cannot do it), the commit of
+// the chunk's keys/values into the k-slot window cache, the cross-entropy
+// combine/mean, the rowsum(dO * O) term of the attention backward, and the
+// token pick of decoding.  (RoPE's transpose runs in the attention backward.)
 //
 // All are HBM-bound: one warp per row, 16-byte vector loads/stores, fp32
 // arithmetic; operands for the tensor-core kernels are written as bf16
@@ -254,35 +255,6 @@ __global__ void rope_qkv_kernel(const float* __restrict__ qkv, const float* __re
       vl[o1 + j] = l1;
       vl[o2 + j] = l2;
     }
-  }
-}
-
-// Backward of the rotation (its transpose) for dq, dk; dv passes through.
-// Writes the concatenated [dq | dk | dv] rows (bf16 hi/lo) for the QKV dX product.
-__global__ void rope_bwd_kernel(const float* __restrict__ dq, const float* __restrict__ dk,
-                                const float* __restrict__ dv, const float* __restrict__ cs,
-                                const float* __restrict__ sn, int n, int H, int dh, bf16* oh, bf16* ol) {
-  pdl_wait();
-  pdl_launch_dependents();
-  const int half = dh / 2;
-  const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= (long)n * H * half) return;
-  const int i = (int)(idx % half);
-  const int h = (int)((idx / half) % H);
-  const int t = (int)(idx / ((long)half * H));
-  const int d = H * dh;
-  const float c = cs[(long)t * half + i], s = sn[(long)t * half + i];
-  const long src1 = (long)t * d + h * dh + i, src2 = src1 + half;
-  const long dst = (long)t * 3 * d + h * dh + i;
-  const float q1 = dq[src1], q2 = dq[src2], k1 = dk[src1], k2 = dk[src2];
-  {
-    __nv_bfloat16 a, b;
-    split_bf16(q1 * c + q2 * s, a, b); oh[dst] = a; if (ol) ol[dst] = b;
-    split_bf16(q2 * c - q1 * s, a, b); oh[dst + half] = a; if (ol) ol[dst + half] = b;
-    split_bf16(k1 * c + k2 * s, a, b); oh[dst + d] = a; if (ol) ol[dst + d] = b;
-    split_bf16(k2 * c - k1 * s, a, b); oh[dst + d + half] = a; if (ol) ol[dst + d + half] = b;
-    split_bf16(dv[src1], a, b); oh[dst + 2 * d] = a; if (ol) ol[dst + 2 * d] = b;
-    split_bf16(dv[src2], a, b); oh[dst + 2 * d + half] = a; if (ol) ol[dst + 2 * d + half] = b;
   }
 }
 
@@ -559,12 +531,6 @@ int rows_rope_qkv(const float* qkv, const float* cs, const float* sn, int n, int
                   bf16* kh, bf16* kl, bf16* vh, bf16* vl, cudaStream_t st) {
   const long tot = (long)n * H * (dh / 8);
   return (int)launch_k(rope_qkv_kernel, dim3((unsigned)((tot + 255) / 256)), dim3(256), 0, st, qkv, cs, sn, n, H, dh, qh, ql, kh, kl, vh, vl);
-}
-
-int rows_rope_bwd(const float* dq, const float* dk, const float* dv, const float* cs, const float* sn, int n, int H,
-                  int dh, bf16* oh, bf16* ol, cudaStream_t st) {
-  const long tot = (long)n * H * (dh / 2);
-  return (int)launch_k(rope_bwd_kernel, dim3((unsigned)((tot + 255) / 256)), dim3(256), 0, st, dq, dk, dv, cs, sn, n, H, dh, oh, ol);
 }
 
 int rows_commit(const bf16* own, bf16* ring, long own_layer_stride, long ring_layer_stride, int n_layers, long pos0,

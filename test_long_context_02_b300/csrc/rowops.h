@@ -13,8 +13,6 @@ int rows_rmsnorm_bwd(const float* dy, const float* x, const float* g, const floa
 int rows_rope_table(long pos0, int n, int dh, const double* inv_freq, float* cs, float* sn, cudaStream_t st);
 int rows_rope_qkv(const float* qkv, const float* cs, const float* sn, int n, int H, int dh, bf16* qh, bf16* ql,
                   bf16* kh, bf16* kl, bf16* vh, bf16* vl, cudaStream_t st);
-int rows_rope_bwd(const float* dq, const float* dk, const float* dv, const float* cs, const float* sn, int n, int H,
-                  int dh, bf16* oh, bf16* ol, cudaStream_t st);
 int rows_commit(const bf16* own, bf16* ring, long own_layer_stride, long ring_layer_stride, int n_layers, long pos0,
                 int n, int window, int d, cudaStream_t st);
 int rows_ce_combine(const float2* part, const float* zt, const int* tgt, int n, int ntiles, float* lse,

@@ -95,7 +95,7 @@ struct ttt_ctx {
   Pair xf, dz;
   float *rs_f = nullptr, *zt = nullptr, *lse_row = nullptr, *loss_row = nullptr, *inv_nvalid = nullptr;
   float2* part = nullptr;
-  float *dy = nullptr, *dxn = nullptr, *dh32 = nullptr, *D = nullptr, *dq = nullptr, *dk = nullptr, *dv = nullptr;
+  float *dy = nullptr, *dxn = nullptr, *dh32 = nullptr, *D = nullptr;
   Pair dy16, da, dh16, do16, dqkv;
   float* sa_s = nullptr;     // dual-MLP: static pre-activations [S][b][f]
   float* zdec = nullptr;     // decoding: one row of logits [V]
@@ -564,10 +564,6 @@ int suffix_step(ttt_ctx* c, int s, int row, const int* tok, int n, const int* ne
       ba.g.ldo = d; ba.g.err = c->derr;
       ba.lse = c->slse + (long)si * H * b;
       ba.D = c->D;
-      ba.dq = c->dq;
-      ba.dk = c->dk;
-      ba.dv = c->dv;
-      ba.ldg = d;
       ba.scale = (float)(1.0 / std::sqrt((double)dh));
       // written straight into the QKV dX product's operand, RoPE's rotation transposed
       ba.qkv_h = c->dqkv.hi; ba.qkv_l = c->dqkv.lo; ba.ld_qkv = 3L * d; ba.k_off = d; ba.v_off = 2L * d;
@@ -711,9 +707,6 @@ extern "C" int ttt_create(const ttt_config* cfg, void* cuda_stream, ttt_ctx** ou
   c->dxn = dalloc<float>(c, b * d, ok);
   c->dh32 = dalloc<float>(c, b * d, ok);
   c->D = dalloc<float>(c, H * b, ok);
-  c->dq = dalloc<float>(c, b * d, ok);
-  c->dk = dalloc<float>(c, b * d, ok);
-  c->dv = dalloc<float>(c, b * d, ok);
   c->dy16 = palloc(c, b * d, ok);
   c->da = palloc(c, b * f, ok);
   c->dh16 = palloc(c, b * d, ok);
