@@ -3,16 +3,19 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 760m] [--impl ours|reference]
 
-One step = one whole sequence through the inner loop: for every chunk of b
-tokens, forward through all blocks, next-token cross-entropy, backward through
-the last quarter of the blocks and the SGD step on their MLP weights, then the
-window-cache commit.  Each step restarts the sequence from the loaded weights
-(ttt_reset, inside the timed region).  value = tokens of all ranks / max over
-ranks of the device time of K steps (CUDA events on the library's stream).
+One step = every sequence of the workload's context (one for the 125M, 760M
+and 3B workloads, four for the window/chunk sweep) through the inner loop:
+for every chunk of b tokens, forward through all blocks, next-token
+cross-entropy, backward through the last quarter of the blocks and the SGD
+step on their MLP weights, then the window-cache commit.  Each step restarts
+the sequences from the loaded weights (ttt_reset, inside the timed region).
+value = tokens of all ranks / max over ranks of the device time of K steps
+(CUDA events on the library's stream).
 
 Multi-GPU: the inner loop is a serial chain within a sequence, so ranks are
-independent replicas (one sequence each, seed 1000 + rank); the only
-collectives are the timing barrier and the max-reduction of the elapsed time.
+independent replicas (their own sequences, seeds 1000 + rank*n_seqs + q); the
+only collectives are the timing barrier and the max-reduction of the elapsed
+time.
 
 --impl reference times the float64 oracle (the method as written, numpy) on
 the host cores on a bounded sample of the same workload.
@@ -38,7 +41,7 @@ from ttt_inputs import SHAPES, sequence_tokens, weight_blob  # noqa: E402
 
 METRIC = "TTT prefill tokens/sec at 1 B300; % of bf16 tensor-core roofline"
 UNIT = "tokens/s"
-DATA = "synthetic: Zipf(1.1) token ids with repeated 32-token spans (seed 1000+rank), N(0,0.02) weights (seed 0)"
+DATA = "synthetic: Zipf(1.1) token ids with repeated 32-token spans (sequence q of rank r: seed 1000 + r*n_seqs + q), N(0,0.02) weights (seed 0)"
 
 
 def peaks():
@@ -229,18 +232,19 @@ def run_ours(a):
         if dist is not None:
             dist.barrier()
 
-    shape = SHAPES[a.workload].replace(n_seqs=1)
+    shape = SHAPES[a.workload]
     if a.tokens:
         shape = shape.replace(seq_len=a.tokens)
-    Tn, b = shape.seq_len, shape.chunk
+    # one step = every sequence of the workload's context (the window/chunk sweep holds 4)
+    Tn, b, B = shape.seq_len, shape.chunk, shape.n_seqs
     nc = math.ceil(Tn / b)
-    tokens = sequence_tokens(shape, rank)
+    tokens = np.stack([sequence_tokens(shape, rank * B + q) for q in range(B)]).astype(np.int32)
     blob = weight_blob(shape)
     stream = torch.cuda.Stream()
     m = T.TTT.from_shape(shape, stream=stream.cuda_stream)
     m.load_weights(blob)
     d_tok = torch.tensor(tokens, dtype=torch.int32, device="cuda")
-    d_loss = torch.zeros(nc, dtype=torch.float32, device="cuda")
+    d_loss = torch.zeros((B, nc), dtype=torch.float32, device="cuda")
 
     def one_step():
         m.reset()
@@ -293,10 +297,15 @@ def run_ours(a):
     # chunk) is timed the same way as a second figure.
     e2e_steps = max(1, min(a.steps, 2))
     pin_tok = torch.tensor(tokens, dtype=torch.int32).pin_memory()
-    nxt = np.array([tokens[s + b] if s + b < Tn else -1 for s in range(0, Tn, b)], np.int32)
+    # the per-chunk call takes [B][n] tokens of one chunk: the same ids, laid out chunk-major
+    chunk_major = np.concatenate([tokens[:, s:s + b].reshape(-1) for s in range(0, Tn, b)])
+    pin_ctok = torch.tensor(chunk_major, dtype=torch.int32).pin_memory()
+    nxt = np.array([[tokens[q, s + b] if s + b < Tn else -1 for q in range(B)] for s in range(0, Tn, b)], np.int32)
     pin_next = torch.tensor(nxt).pin_memory()
-    pin_loss = torch.zeros(nc, dtype=torch.float32).pin_memory()
-    base_t, base_n, base_l = pin_tok.data_ptr(), pin_next.data_ptr(), pin_loss.data_ptr()
+    pin_loss = torch.zeros((B, nc), dtype=torch.float32).pin_memory()
+    pin_closs = torch.zeros((nc, B), dtype=torch.float32).pin_memory()
+    base_t, base_ct, base_n = pin_tok.data_ptr(), pin_ctok.data_ptr(), pin_next.data_ptr()
+    base_l, base_cl = pin_loss.data_ptr(), pin_closs.data_ptr()
 
     def timed_host(run):
         barrier()
@@ -314,7 +323,7 @@ def run_ours(a):
         for ci in range(nc):
             s0 = ci * b
             n = min(b, Tn - s0)
-            m._check(T.ttt_prefill_chunk(m._h, base_t + 4 * s0, n, base_n + 4 * ci, base_l + 4 * ci),
+            m._check(T.ttt_prefill_chunk(m._h, base_ct + 4 * B * s0, n, base_n + 4 * B * ci, base_cl + 4 * B * ci),
                      "ttt_prefill_chunk")
 
     e2e_s = timed_host(lambda: m._check(T.ttt_prefill_sequence(m._h, base_t, Tn, base_l), "ttt_prefill_sequence"))
@@ -322,11 +331,13 @@ def run_ours(a):
     if not np.allclose(e2e_losses, losses, rtol=1e-3):
         raise RuntimeError(f"host-buffer sequence losses differ from the device-resident run: {e2e_losses} {losses}")
     e2e_chunk_s = timed_host(per_chunk)
+    if not np.allclose(pin_closs.numpy().T, losses, rtol=1e-3):
+        raise RuntimeError("per-chunk losses differ from the device-resident run")
 
     # --------------------------------------------------------------- reporting (rank 0)
     pk = peaks()
-    alg = algorithmic_flops(shape, Tn)
-    value = replica_tokens_per_s(world, a.steps, Tn, ms_max / 1e3)
+    alg = B * algorithmic_flops(shape, Tn)
+    value = replica_tokens_per_s(world, a.steps, B * Tn, ms_max / 1e3)
     tc_frac = alg * a.steps / (ms / 1e3) / (pk["tc_sus"] * 1e12)
     total_ms = sum(v["ms"] for v in prof.values())
     avg_launch_ms = dom["ms"] / dom["launches"]
@@ -365,28 +376,30 @@ def run_ours(a):
     out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
            "ms_per_step": ms_max / a.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
            "dtype": "bf16" if shape.compute == "bf16" else "f32", "data": DATA,
-           "config": {"workload": workload_name(shape), "tokens_per_step_per_gpu": Tn, "chunks": nc,
+           "config": {"workload": workload_name(shape), "tokens_per_step_per_gpu": B * Tn, "sequences": B,
+                      "chunks": nc,
                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                       "l2": "working set larger than L2 (bf16 weights + window cache > 2 GB), no flush",
                       "timing": "CUDA events on the library stream; inside the timed region (the "
-                                "context's three streams overlapping, as the library runs by default) only "
+                                "context's streams overlapping, three per sequence lane, as the library runs "
+                                "by default) only "
                                 "the dominant kernel class is bracketed by events, on the stream each launch "
                                 "goes to; the per-class table and roofline_isolated come from one extra "
                                 "step with every launch bracketed and the streams in issue order",
-                      "alg_gflop_per_token": alg / Tn / 1e9},
+                      "alg_gflop_per_token": alg / (B * Tn) / 1e9},
            "tc_roofline_frac": tc_frac,
            "tc_roofline_frac_of_burst": tc_frac * pk["tc_sus"] / pk["tc"],
            "roofline": roof, "roofline_isolated": roof_iso, "kernels": kernels, "clocks": clk, "gpu_launches": launches,
-           "e2e": {"value": replica_tokens_per_s(world, e2e_steps, Tn, e2e_s), "unit": UNIT,
-                   "h2d_bytes_per_step": 4 * Tn, "d2h_bytes_per_step": 4 * nc,
+           "e2e": {"value": replica_tokens_per_s(world, e2e_steps, B * Tn, e2e_s), "unit": UNIT,
+                   "h2d_bytes_per_step": 4 * B * Tn, "d2h_bytes_per_step": 4 * B * nc,
                    "api": "ttt_prefill_sequence, pinned host buffers (one upload, one download)",
-                   "per_chunk_api": {"value": replica_tokens_per_s(world, e2e_steps, Tn, e2e_chunk_s),
-                                     "h2d_bytes_per_step": 4 * Tn + 4 * nc, "d2h_bytes_per_step": 4 * nc,
+                   "per_chunk_api": {"value": replica_tokens_per_s(world, e2e_steps, B * Tn, e2e_chunk_s),
+                                     "h2d_bytes_per_step": 4 * B * (Tn + nc), "d2h_bytes_per_step": 4 * B * nc,
                                      "api": "ttt_prefill_chunk per chunk, pinned host buffers"}},
-           "final_chunk_loss": float(losses[-1])}
+           "final_chunk_loss": float(losses[0, -1])}
     if world == 1 and not a.no_cpu_baseline:
         n_tok = a.cpu_tokens or 512
-        v, cores, dt = cpu_sample(shape, blob, tokens, n_tok)
+        v, cores, dt = cpu_sample(shape, blob, tokens[0], n_tok)
         out["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
                                "sample": f"first {n_tok} tokens as one inner-loop step, {dt:.1f} s"}
     print(json.dumps(out), flush=True)

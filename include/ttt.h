@@ -19,7 +19,11 @@
  *
  * Ownership: the context owns all device memory.  Host pointers passed in are
  * read or written only during the call and never retained.
- * Streams: all work is enqueued on the stream given to ttt_create.
+ * Streams: all work is ordered on the stream given to ttt_create.  Inside a
+ * call the context may fork work onto streams of its own (side streams of one
+ * sequence; one lane of streams per sequence, up to 4 sequences at a time) and
+ * joins them back into that stream before the call returns, so later work on
+ * the given stream sees every result.
  * Devices and threads: one process drives one GPU.  The library caches launch
  * settings (per-kernel shared-memory limits, the SM count) on first use, so
  * every context of a process must live on the same device, and calls that
@@ -224,11 +228,13 @@ TTT_API int ttt_reset(ttt_ctx* ctx);
  * on = 1 (the default): within a sequence, the frozen-block pass of the next
  * group of chunks runs on a second stream of the context beside the current
  * group's trainable steps, and the fast-weight gradient products with their SGD
- * step run on a third stream beside the rest of each chunk's backward.
- * on = 0: every kernel runs on the context stream in issue order (per-kernel
- * timings then measure each kernel alone).  Results are the same either way,
- * up to the summation order of K-sliced products.  Synchronises the context
- * stream; returns TTT_ERR_ARG for another value.
+ * step run on a third stream beside the rest of each chunk's backward; with
+ * several sequences, up to 4 of them run side by side, each on its own lane
+ * (working buffers and streams), their launches enqueued chunk by chunk in turn.
+ * on = 0: every kernel runs on the context stream in issue order, one sequence
+ * after another (per-kernel timings then measure each kernel alone).  Results
+ * are the same either way, up to the summation order of K-sliced products.
+ * Synchronises the context stream; returns TTT_ERR_ARG for another value.
  */
 TTT_API int ttt_set_concurrency(ttt_ctx* ctx, int32_t on);
 

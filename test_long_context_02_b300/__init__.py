@@ -302,7 +302,7 @@ class TTT:
         self._check(ttt_import_state(self._h, seq, buf.ctypes.data, buf.size), "ttt_import_state")
 
     def set_concurrency(self, on: bool):
-        """Second/third-stream overlap inside the context (on by default); off runs in issue order."""
+        """Side streams and side-by-side sequences inside the context (on by default); off runs in issue order."""
         self._check(ttt_set_concurrency(self._h, 1 if on else 0), "ttt_set_concurrency")
 
     def reset(self):

@@ -4,10 +4,12 @@
 // the fp32-compute mode) and n_seqs independent sequences, each with its own
 // k-slot key/value window cache per layer and its own fp32 fast weights
 // (W_up, W_down of the last S blocks) with bf16 shadows used as GEMM operands.
+// Up to kMaxLanes sequences run side by side, each on a lane: its own working
+// buffers and streams, forked from the context stream and joined back into it.
 //
 // One inner-loop step of one sequence (pages: "把 Transformer 做成“终身学习者”：
 // TTT-E2E 如何让大模型边用边学？", §4.2 and §4.4; "TTT-E2E技术：突破大语言模型上下文限制的新范式",
-// §2.1), all on the context stream:
+// §2.1), all on the lane's main stream unless noted:
 //   forward  : embed; per block RMSNorm, QKV product, RoPE (+ own K/V), windowed
 //              attention, O product + residual, RMSNorm, up product + GELU,
 //              down product + residual; final RMSNorm; LM head fused with the
@@ -53,6 +55,41 @@ struct Seq {
   Pair up16, down16;            // shadows
 };
 
+// Per-sequence working set of the chunk loop.  A lane runs one sequence at a
+// time; a context with several sequences runs them on several lanes, each on
+// its own streams, side by side on the GPU (lane 0's main stream is the
+// context stream; the others fork from it and join back into it).
+struct Lane {
+  cudaStream_t st = nullptr;  // main stream of the lane
+  bool own_st = false;        // st was created for the lane (lanes other than 0)
+  int* tgt = nullptr;
+  float *cs = nullptr, *sn = nullptr;
+  float *x = nullptr, *xp = nullptr, *qkv = nullptr;
+  Pair xn, q, o, u;
+  // frozen-prefix pass outputs, double-buffered so the pass of the next group of chunks
+  // can run on a second stream while the current group's trainable steps read theirs
+  float* xpb[2] = {nullptr, nullptr};   // [R][d] residual stream after the frozen blocks (xpb[0] == xp)
+  float* csb[2] = {nullptr, nullptr};   // angle tables [R][dh/2] (csb[0] == cs, snb[0] == sn)
+  float* snb[2] = {nullptr, nullptr};
+  Pair sxn;                             // [b][d] normalised attention input of the trainable blocks
+  cudaStream_t st2 = nullptr;           // the frozen-prefix passes run ahead on this stream
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr, ev_pass[2] = {nullptr, nullptr}, ev_suf[2] = {nullptr, nullptr};
+  // the fast-weight gradient products with their SGD step run on a third stream beside
+  // the rest of the chunk's backward (nothing in it reads the updated weights)
+  cudaStream_t st3 = nullptr;
+  cudaEvent_t ev_da = nullptr, ev_dx = nullptr, ev_wd = nullptr, ev_wu = nullptr;
+  Pair kown, vown;           // [L][R][d]
+  float *sx = nullptr, *sh = nullptr, *srs_a = nullptr, *srs_m = nullptr, *slse = nullptr, *sa = nullptr;
+  Pair sq, so, sxm, su;
+  Pair xf, dz;
+  float *rs_f = nullptr, *zt = nullptr, *lse_row = nullptr, *loss_row = nullptr, *inv_nvalid = nullptr;
+  float2* part = nullptr;
+  float *dy = nullptr, *dxn = nullptr, *dh32 = nullptr, *D = nullptr;
+  Pair dy16, da, dh16, do16, dqkv;
+  float* sa_s = nullptr;     // dual-MLP: static pre-activations [S][b][f]
+  Pair us, da_s;             // dual-MLP: static GELU output and its gradient [b][f]
+};
+
 }  // namespace
 
 struct ttt_ctx {
@@ -69,37 +106,14 @@ struct ttt_ctx {
   Pair Wqkv, Wo, Wup, Wdown, Wlm;  // [L][d][3d], [L][d][d], [L-S][d][f], [L-S][f][d], [d][V]
   Pair Wup_s, Wdown_s;             // dual-MLP variant: static pair of the trainable blocks [S][d][f], [S][f][d]
   std::vector<Seq> seqs;
-  // per-step device scratch
-  int *tok = nullptr, *tgt = nullptr, *next = nullptr, *minus1 = nullptr, *derr = nullptr;
+  std::vector<Lane> lanes;         // min(n_seqs, kMaxLanes) working sets
+  bool concurrent = true;  // side streams and parallel lanes (ttt_set_concurrency)
+  // per-call device scratch shared by the lanes
+  int *tok = nullptr, *next = nullptr, *minus1 = nullptr, *derr = nullptr;
   float* loss_dev = nullptr;
   double* inv_freq = nullptr;
-  float *cs = nullptr, *sn = nullptr;
-  float *x = nullptr, *xp = nullptr, *qkv = nullptr;
-  Pair xn, q, o, u;
-  // frozen-prefix pass outputs, double-buffered so the pass of the next group of chunks
-  // can run on a second stream while the current group's trainable steps read theirs
-  float* xpb[2] = {nullptr, nullptr};   // [R][d] residual stream after the frozen blocks (xpb[0] == xp)
-  float* csb[2] = {nullptr, nullptr};   // angle tables [R][dh/2] (csb[0] == cs, snb[0] == sn)
-  float* snb[2] = {nullptr, nullptr};
-  Pair sxn;                             // [b][d] normalised attention input of the trainable blocks
-  cudaStream_t st2 = nullptr;           // the frozen-prefix passes run ahead on this stream
-  cudaEvent_t ev_fork = nullptr, ev_pass[2] = {nullptr, nullptr}, ev_suf[2] = {nullptr, nullptr};
-  // the fast-weight gradient products with their SGD step run on a third stream beside
-  // the rest of the chunk's backward (nothing in it reads the updated weights)
-  cudaStream_t st3 = nullptr;
-  cudaEvent_t ev_da = nullptr, ev_dx = nullptr, ev_wd = nullptr, ev_wu = nullptr;
-  bool concurrent = true;  // use the second and third streams (ttt_set_concurrency)
-  Pair kown, vown;           // [L][R][d]
-  float *sx = nullptr, *sh = nullptr, *srs_a = nullptr, *srs_m = nullptr, *slse = nullptr, *sa = nullptr;
-  Pair sq, so, sxm, su;
-  Pair xf, dz;
-  float *rs_f = nullptr, *zt = nullptr, *lse_row = nullptr, *loss_row = nullptr, *inv_nvalid = nullptr;
-  float2* part = nullptr;
-  float *dy = nullptr, *dxn = nullptr, *dh32 = nullptr, *D = nullptr;
-  Pair dy16, da, dh16, do16, dqkv;
-  float* sa_s = nullptr;     // dual-MLP: static pre-activations [S][b][f]
   float* zdec = nullptr;     // decoding: one row of logits [V]
-  Pair us, da_s;             // dual-MLP: static GELU output and its gradient [b][f]
+  cudaEvent_t ev_fork = nullptr;  // lanes and side streams start after the context stream's earlier work
   // host whole-sequence entry point: device staging of tokens and losses (grown on demand)
   int* seq_tok = nullptr;
   float* seq_loss = nullptr;
@@ -130,6 +144,8 @@ namespace {
 
 // Rows of one frozen-prefix pass (whole chunks): large enough for full GEMM waves.
 constexpr int kPrefixRows = 8192;
+// Sequences of one context that run side by side (each lane holds one working set).
+constexpr int kMaxLanes = 4;
 
 int fail(ttt_ctx* c, int code, const std::string& msg) {
   if (c) c->err = msg;
@@ -264,25 +280,25 @@ double tile_pairs(long pos0, int n, int k) {
 // run with save = true (r0 = 0) keep what their backward needs in the suffix
 // buffers and write xout.  si >= 0 selects the sequence's fast weights.
 // xin / xout and the angle tables cs / sn point at row r0.
-int layer_forward(ttt_ctx* c, Seq& sq_, int l, int si, bool save, int n, int r0, long pos0, float* xin,
+int layer_forward(ttt_ctx* c, Lane& ln, Seq& sq_, int l, int si, bool save, int n, int r0, long pos0, float* xin,
                   float* xout, const float* cs, const float* sn, cudaStream_t st) {
   const int d = c->d, H = c->H, dh = c->dh, f = c->f, k = c->k, b = c->b, R = c->R;
   const bool fast = si >= 0, suf = fast && save, sp = c->split;
   const double nn = n, dd = d, ff = f;
   const double ops = sp ? 3.0 : 1.0, eb = sp ? 4.0 : 2.0;
   const long ro = (long)r0 * d, rf = (long)r0 * f;
-  float* hbuf = suf ? c->sh + (long)si * b * d : xin;
-  Pair xn_a = suf ? c->sxn : c->xn.at(ro);
-  Pair q0 = suf ? c->sq.at((long)si * b * d) : c->q;  // row 0 of the chunk's queries / outputs
-  Pair o0 = suf ? c->so.at((long)si * b * d) : c->o;
-  Pair xn_m = suf ? c->sxm.at((long)si * b * d) : c->xn.at(ro);
-  Pair ub = suf ? c->su.at((long)si * b * f) : c->u.at(rf);
-  Pair ko0 = c->kown.at((long)l * R * d), vo0 = c->vown.at((long)l * R * d);
+  float* hbuf = suf ? ln.sh + (long)si * b * d : xin;
+  Pair xn_a = suf ? ln.sxn : ln.xn.at(ro);
+  Pair q0 = suf ? ln.sq.at((long)si * b * d) : ln.q;  // row 0 of the chunk's queries / outputs
+  Pair o0 = suf ? ln.so.at((long)si * b * d) : ln.o;
+  Pair xn_m = suf ? ln.sxm.at((long)si * b * d) : ln.xn.at(ro);
+  Pair ub = suf ? ln.su.at((long)si * b * f) : ln.u.at(rf);
+  Pair ko0 = ln.kown.at((long)l * R * d), vo0 = ln.vown.at((long)l * R * d);
   Pair kr = sq_.ring_k.at((long)l * k * d), vr = sq_.ring_v.at((long)l * k * d);
 
   RUN(K_RMSNORM, 1, 0, 0, nn * dd * (4 + eb),
       rows_rmsnorm(xin, c->gains + (long)(2 * l) * d, c->cfg.rms_eps, n, d, xn_a.hi, xn_a.lo,
-                   suf ? c->srs_a + (long)si * b : nullptr, st));
+                   suf ? ln.srs_a + (long)si * b : nullptr, st));
   Pair qw = q0.at(ro), kw = ko0.at(ro), vw = vo0.at(ro);
   if (qkv_rope_bn(dh, d, sp)) {  // RoPE and the q / own k / own v writes fused into the product's epilogue
     GemmArgs g;
@@ -294,11 +310,11 @@ int layer_forward(ttt_ctx* c, Seq& sq_, int l, int si, bool save, int n, int r0,
   } else {
     GemmArgs g;
     g.M = n; g.N = 3 * d; g.K = d;
-    g.out32 = c->qkv; g.ldo32 = 3 * d; g.err = c->derr;
+    g.out32 = ln.qkv; g.ldo32 = 3 * d; g.err = c->derr;
     RUN(K_GEMM_QKV, 1, 6 * nn * dd * dd, 6 * nn * dd * dd * ops, 0,
         gemm_run(EPI_F32, opnd(xn_a, d, 0), opnd(c->Wqkv.at((long)l * d * 3 * d), 3 * d, 1), g, sp, st));
     RUN(K_ROPE, 1, 0, 0, nn * dd * (12 + 3 * eb),
-        rows_rope_qkv(c->qkv, cs, sn, n, H, dh, qw.hi, qw.lo, kw.hi, kw.lo, vw.hi, vw.lo, st));
+        rows_rope_qkv(ln.qkv, cs, sn, n, H, dh, qw.hi, qw.lo, kw.hi, kw.lo, vw.hi, vw.lo, st));
   }
   {  // queries r0 .. r0+n-1 over the cache and own keys 0 .. r0+n-1 (tiles before r0's are skipped)
     const int na = r0 + n;
@@ -308,7 +324,7 @@ int layer_forward(ttt_ctx* c, Seq& sq_, int l, int si, bool save, int n, int r0,
     a.n = na; a.H = H; a.dh = dh; a.window = k; a.pos0 = pos0; a.qt0 = r0 / 128;
     a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)dh));
     a.o_hi = o0.hi; a.o_lo = o0.lo; a.ldo = d;
-    a.lse = suf ? c->slse + (long)si * H * b : nullptr;
+    a.lse = suf ? ln.slse + (long)si * H * b : nullptr;
     a.err = c->derr;
     RUN(K_ATTN_FWD, 1, 4 * dd * window_pairs(pos0 + r0, n, k), 4 * dd * tile_pairs(pos0, na, k) * ops, 0,
         attn_fwd_run(m, a, sp, st));
@@ -322,11 +338,11 @@ int layer_forward(ttt_ctx* c, Seq& sq_, int l, int si, bool save, int n, int r0,
   }
   RUN(K_RMSNORM, 1, 0, 0, nn * dd * (4 + eb),
       rows_rmsnorm(hbuf, c->gains + (long)(2 * l + 1) * d, c->cfg.rms_eps, n, d, xn_m.hi, xn_m.lo,
-                   suf ? c->srs_m + (long)si * b : nullptr, st));
+                   suf ? ln.srs_m + (long)si * b : nullptr, st));
   {
     GemmArgs g;
     g.M = n; g.N = f; g.K = d;
-    g.out32 = suf ? c->sa + (long)si * b * f : nullptr;  // pre-activation kept for GELU' only when trainable
+    g.out32 = suf ? ln.sa + (long)si * b * f : nullptr;  // pre-activation kept for GELU' only when trainable
     g.ldo32 = f; g.oh = ub.hi; g.ol = ub.lo; g.ldo = f; g.err = c->derr;
     Pair w = fast ? sq_.up16.at((long)si * d * f) : c->Wup.at((long)l * d * f);
     RUN(K_GEMM_UP, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 0,
@@ -341,10 +357,10 @@ int layer_forward(ttt_ctx* c, Seq& sq_, int l, int si, bool save, int n, int r0,
         gemm_run(EPI_RESID, opnd(ub, f, 0), opnd(w, d, 1), g, sp, st));
   }
   if (fast && c->dual) {  // the frozen static MLP of a trainable block, on the same normalised input
-    Pair usb = c->us.at(rf);
+    Pair usb = ln.us.at(rf);
     GemmArgs g;
     g.M = n; g.N = f; g.K = d;
-    g.out32 = suf ? c->sa_s + (long)si * b * f : nullptr; g.ldo32 = f; g.oh = usb.hi; g.ol = usb.lo; g.ldo = f;
+    g.out32 = suf ? ln.sa_s + (long)si * b * f : nullptr; g.ldo32 = f; g.oh = usb.hi; g.ol = usb.lo; g.ldo = f;
     g.err = c->derr;
     RUN(K_GEMM_UP, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 0,
         gemm_run(EPI_GELU, opnd(xn_m, d, 0), opnd(c->Wup_s.at((long)si * d * f), f, 1), g, sp, st));
@@ -360,30 +376,30 @@ int layer_forward(ttt_ctx* c, Seq& sq_, int l, int si, bool save, int n, int r0,
 // The frozen blocks 0..L-S-1 of sequence s over n tokens (whole chunks, n <= R)
 // starting at absolute position pos0.  Their outputs do not depend on the fast
 // weights, so several chunks go through them in one pass; the suffix steps of
-// those chunks then read their rows of c->xp.  The frozen blocks' keys/values
+// those chunks then read their rows of ln.xp.  The frozen blocks' keys/values
 // of all n tokens enter the window cache at the end of the pass (every query of
 // the pass has already read the cache).
-int prefix_pass(ttt_ctx* c, int s, const int* tok, int n, long pos0, cudaStream_t st, int buf) {
+int prefix_pass(ttt_ctx* c, Lane& ln, int s, const int* tok, int n, long pos0, cudaStream_t st, int buf) {
   Seq& sq_ = c->seqs[s];
-  float* xp = c->xpb[buf];
+  float* xp = ln.xpb[buf];
   const int d = c->d, dh = c->dh, k = c->k, R = c->R;
   const int P0 = c->L - c->S;
   const double nn = n, dd = d;
   RUN(K_MISC, 1, 0, 0, nn * dd * 8, rows_embed(tok, n, c->E, c->V, d, xp, c->derr, st));
-  RUN(K_ROPE, 1, 0, 0, nn * dh * 4, rows_rope_table(pos0, n, dh, c->inv_freq, c->csb[buf], c->snb[buf], st));
+  RUN(K_ROPE, 1, 0, 0, nn * dh * 4, rows_rope_table(pos0, n, dh, c->inv_freq, ln.csb[buf], ln.snb[buf], st));
   for (int l = 0; l < P0; ++l) {
-    const int r = layer_forward(c, sq_, l, -1, false, n, 0, pos0, xp, xp, c->csb[buf], c->snb[buf], st);
+    const int r = layer_forward(c, ln, sq_, l, -1, false, n, 0, pos0, xp, xp, ln.csb[buf], ln.snb[buf], st);
     if (r != TTT_OK) return r;
   }
   if (P0 > 0) {
     const double cb = (double)P0 * nn * dd * 2 * 2;
-    RUN(K_COMMIT, 1, 0, 0, cb, rows_commit(c->kown.hi, sq_.ring_k.hi, (long)R * d, (long)k * d, P0, pos0, n, k, d, st));
-    RUN(K_COMMIT, 1, 0, 0, cb, rows_commit(c->vown.hi, sq_.ring_v.hi, (long)R * d, (long)k * d, P0, pos0, n, k, d, st));
+    RUN(K_COMMIT, 1, 0, 0, cb, rows_commit(ln.kown.hi, sq_.ring_k.hi, (long)R * d, (long)k * d, P0, pos0, n, k, d, st));
+    RUN(K_COMMIT, 1, 0, 0, cb, rows_commit(ln.vown.hi, sq_.ring_v.hi, (long)R * d, (long)k * d, P0, pos0, n, k, d, st));
     if (c->split) {
       RUN(K_COMMIT, 1, 0, 0, cb,
-          rows_commit(c->kown.lo, sq_.ring_k.lo, (long)R * d, (long)k * d, P0, pos0, n, k, d, st));
+          rows_commit(ln.kown.lo, sq_.ring_k.lo, (long)R * d, (long)k * d, P0, pos0, n, k, d, st));
       RUN(K_COMMIT, 1, 0, 0, cb,
-          rows_commit(c->vown.lo, sq_.ring_v.lo, (long)R * d, (long)k * d, P0, pos0, n, k, d, st));
+          rows_commit(ln.vown.lo, sq_.ring_v.lo, (long)R * d, (long)k * d, P0, pos0, n, k, d, st));
     }
   }
   return TTT_OK;
@@ -393,9 +409,9 @@ int prefix_pass(ttt_ctx* c, int s, const int* tok, int n, long pos0, cudaStream_
 // within the last prefix pass: tokens tok[n], next target next[1] (device).
 // Runs the trainable blocks forward, the loss, the backward through them with
 // the fused SGD step, and commits their keys/values; the position advances by n.
-int suffix_step(ttt_ctx* c, int s, int row, const int* tok, int n, const int* next, float* loss_out, int buf = 0) {
+int suffix_step(ttt_ctx* c, Lane& ln, int s, int row, const int* tok, int n, const int* next, float* loss_out, int buf = 0) {
   Seq& sq_ = c->seqs[s];
-  cudaStream_t st = c->st;
+  cudaStream_t st = ln.st;
   const int L = c->L, S = c->S, d = c->d, H = c->H, dh = c->dh, f = c->f, V = c->V, k = c->k, b = c->b, R = c->R;
   const long pos0 = sq_.pos;
   const bool sp = c->split;
@@ -408,152 +424,152 @@ int suffix_step(ttt_ctx* c, int s, int row, const int* tok, int n, const int* ne
   const double own_pairs = nn * (nn + 1) / 2;
   const int nq = (n + 127) / 128;
   const double own_tile_pairs = 128.0 * 128.0 * nq * (nq + 1) / 2;
-  const float* cs = c->csb[buf] + (long)row * (dh / 2);
-  const float* sn = c->snb[buf] + (long)row * (dh / 2);
+  const float* cs = ln.csb[buf] + (long)row * (dh / 2);
+  const float* sn = ln.snb[buf] + (long)row * (dh / 2);
 
-  RUN(K_MISC, 1, 0, 0, nn * 8, rows_targets(tok, n, next, V, c->tgt, c->derr, st));
+  RUN(K_MISC, 1, 0, 0, nn * 8, rows_targets(tok, n, next, V, ln.tgt, c->derr, st));
 
   // ------------------------------------------------------------------ forward
   for (int l = P0; l < L; ++l) {
     const int si = l - P0;
-    float* xin = si == 0 ? c->xpb[buf] + (long)row * d : c->sx + (long)si * b * d;
-    float* xout = (l + 1 < L) ? c->sx + (long)(si + 1) * b * d : c->x;
-    const int r = layer_forward(c, sq_, l, si, true, n, 0, pos0, xin, xout, cs, sn, st);
+    float* xin = si == 0 ? ln.xpb[buf] + (long)row * d : ln.sx + (long)si * b * d;
+    float* xout = (l + 1 < L) ? ln.sx + (long)(si + 1) * b * d : ln.x;
+    const int r = layer_forward(c, ln, sq_, l, si, true, n, 0, pos0, xin, xout, cs, sn, st);
     if (r != TTT_OK) return r;
   }
   // final norm + LM head + cross-entropy statistics
   RUN(K_RMSNORM, 1, 0, 0, nn * dd * (4 + eb),
-      rows_rmsnorm(c->x, c->gains + (long)(2 * L) * d, c->cfg.rms_eps, n, d, c->xf.hi, c->xf.lo, c->rs_f, st));
+      rows_rmsnorm(ln.x, c->gains + (long)(2 * L) * d, c->cfg.rms_eps, n, d, ln.xf.hi, ln.xf.lo, ln.rs_f, st));
   const int bn = pick_bn(n, V);
   const int ntiles = (V + bn - 1) / bn;
   {
     GemmArgs g;
     g.M = n; g.N = V; g.K = d;
-    g.tgt = c->tgt; g.part = c->part; g.zt = c->zt; g.err = c->derr;
+    g.tgt = ln.tgt; g.part = ln.part; g.zt = ln.zt; g.err = c->derr;
     RUN(K_CE_FWD, 1, 2 * nn * dd * VV, 2 * nn * dd * VV * ops, 0,
-        gemm_run(EPI_CE_FWD, opnd(c->xf, d, 0), opnd(c->Wlm, V, 1), g, sp, st));
+        gemm_run(EPI_CE_FWD, opnd(ln.xf, d, 0), opnd(c->Wlm, V, 1), g, sp, st));
   }
   RUN(K_MISC, 1, 0, 0, nn * ntiles * 8,
-      rows_ce_combine(c->part, c->zt, c->tgt, n, ntiles, c->lse_row, c->loss_row, st));
-  RUN(K_MISC, 1, 0, 0, nn * 8, rows_loss_mean(c->loss_row, c->tgt, n, loss_out, c->inv_nvalid, st));
+      rows_ce_combine(ln.part, ln.zt, ln.tgt, n, ntiles, ln.lse_row, ln.loss_row, st));
+  RUN(K_MISC, 1, 0, 0, nn * 8, rows_loss_mean(ln.loss_row, ln.tgt, n, loss_out, ln.inv_nvalid, st));
 
   // ----------------------------------------------------------------- backward
   {  // dZ = (softmax(Z) - onehot(target)) / n_valid, logits recomputed tile by tile
     GemmArgs g;
     g.M = n; g.N = V; g.K = d;
-    g.tgt = c->tgt; g.lse = c->lse_row; g.scale_dev = c->inv_nvalid;
-    g.oh = c->dz.hi; g.ol = c->dz.lo; g.ldo = V; g.err = c->derr;
+    g.tgt = ln.tgt; g.lse = ln.lse_row; g.scale_dev = ln.inv_nvalid;
+    g.oh = ln.dz.hi; g.ol = ln.dz.lo; g.ldo = V; g.err = c->derr;
     RUN(K_CE_BWD, 1, 0, 2 * nn * dd * VV * ops, 0,
-        gemm_run(EPI_CE_BWD, opnd(c->xf, d, 0), opnd(c->Wlm, V, 1), g, sp, st));
+        gemm_run(EPI_CE_BWD, opnd(ln.xf, d, 0), opnd(c->Wlm, V, 1), g, sp, st));
   }
   {
     GemmArgs g;
     g.M = n; g.N = d; g.K = V;
-    g.out32 = c->dxn; g.ldo32 = d; g.err = c->derr; g.allow_ksplit = true;
+    g.out32 = ln.dxn; g.ldo32 = d; g.err = c->derr; g.allow_ksplit = true;
     RUN(K_LM_DX, 1, 2 * nn * dd * VV, 2 * nn * dd * VV * ops, 0,
-        gemm_run(EPI_F32, opnd(c->dz, V, 0), opnd(c->Wlm, V, 0), g, sp, st));
+        gemm_run(EPI_F32, opnd(ln.dz, V, 0), opnd(c->Wlm, V, 0), g, sp, st));
   }
   RUN(K_RMSNORM, 1, 0, 0, nn * dd * (12 + eb),
-      rows_rmsnorm_bwd(c->dxn, c->x, c->gains + (long)(2 * L) * d, c->rs_f, nullptr, n, d, c->dy, c->dy16.hi,
-                       c->dy16.lo, st));
+      rows_rmsnorm_bwd(ln.dxn, ln.x, c->gains + (long)(2 * L) * d, ln.rs_f, nullptr, n, d, ln.dy, ln.dy16.hi,
+                       ln.dy16.lo, st));
   // The dW + SGD products go to the third stream when it is free to run beside the rest:
   //   W_down step after dA (which reads W_down and dY)      -> before dY is overwritten
   //   W_up step after dXn (which reads W_up) and dA        -> before dA is overwritten
   //   all steps done before the chunk ends (the next chunk's forward reads the weights).
-  const bool side = c->st3 != nullptr && c->concurrent;
-  cudaStream_t sw = side ? c->st3 : st;
+  const bool side = ln.st3 != nullptr && c->concurrent;
+  cudaStream_t sw = side ? ln.st3 : st;
   bool wd_pending = false, wu_pending = false;
   for (int si = S - 1; si >= 0; --si) {
     const int l = P0 + si;
     Pair up16 = sq_.up16.at((long)si * d * f), down16 = sq_.down16.at((long)si * f * d);
     if (wu_pending) {  // the previous block's W_up step has read dA
-      CK(cudaStreamWaitEvent(st, c->ev_wu, 0));
+      CK(cudaStreamWaitEvent(st, ln.ev_wu, 0));
       wu_pending = false;
     }
     {  // dA = (dY W_down^T) * gelu'(a)
       GemmArgs g;
       g.M = n; g.N = f; g.K = d;
-      g.aux = c->sa + (long)si * b * f; g.ldaux = f;
-      g.oh = c->da.hi; g.ol = c->da.lo; g.ldo = f; g.err = c->derr;
+      g.aux = ln.sa + (long)si * b * f; g.ldaux = f;
+      g.oh = ln.da.hi; g.ol = ln.da.lo; g.ldo = f; g.err = c->derr;
       RUN(K_MLP_DX, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 0,
-          gemm_run(EPI_GELU_BWD, opnd(c->dy16, d, 0), opnd(down16, d, 0), g, sp, st));
+          gemm_run(EPI_GELU_BWD, opnd(ln.dy16, d, 0), opnd(down16, d, 0), g, sp, st));
     }
     {  // W_down -= eta U^T dY
       if (side) {
-        CK(cudaEventRecord(c->ev_da, st));
-        CK(cudaStreamWaitEvent(sw, c->ev_da, 0));
+        CK(cudaEventRecord(ln.ev_da, st));
+        CK(cudaStreamWaitEvent(sw, ln.ev_da, 0));
       }
       GemmArgs g;
       g.M = f; g.N = d; g.K = n;
       g.w32 = sq_.down32 + (long)si * f * d; g.wh = down16.hi; g.wl = down16.lo; g.ldw = d; g.eta = eta;
       g.err = c->derr;
       RUN_ON(sw, K_DW_SGD, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 8 * dd * ff,
-             gemm_run(EPI_SGD, opnd(c->su.at((long)si * b * f), f, 1), opnd(c->dy16, d, 1), g, sp, sw));
+             gemm_run(EPI_SGD, opnd(ln.su.at((long)si * b * f), f, 1), opnd(ln.dy16, d, 1), g, sp, sw));
       if (side) {
-        CK(cudaEventRecord(c->ev_wd, sw));
+        CK(cudaEventRecord(ln.ev_wd, sw));
         wd_pending = true;
       }
     }
     if (si > 0) {  // dXn_m = dA W_up^T  (before W_up changes)
       GemmArgs g;
       g.M = n; g.N = d; g.K = f;
-      g.out32 = c->dxn; g.ldo32 = d; g.err = c->derr; g.allow_ksplit = true;
+      g.out32 = ln.dxn; g.ldo32 = d; g.err = c->derr; g.allow_ksplit = true;
       RUN(K_MLP_DX, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 0,
-          gemm_run(EPI_F32, opnd(c->da, f, 0), opnd(up16, f, 0), g, sp, st));
+          gemm_run(EPI_F32, opnd(ln.da, f, 0), opnd(up16, f, 0), g, sp, st));
     }
     if (si > 0 && c->dual) {  // the static MLP passes gradient to its input: dXn_m += dA_s W_up_s^T
       GemmArgs g;
       g.M = n; g.N = f; g.K = d;
-      g.aux = c->sa_s + (long)si * b * f; g.ldaux = f;
-      g.oh = c->da_s.hi; g.ol = c->da_s.lo; g.ldo = f; g.err = c->derr;
+      g.aux = ln.sa_s + (long)si * b * f; g.ldaux = f;
+      g.oh = ln.da_s.hi; g.ol = ln.da_s.lo; g.ldo = f; g.err = c->derr;
       RUN(K_MLP_DX, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 0,
-          gemm_run(EPI_GELU_BWD, opnd(c->dy16, d, 0), opnd(c->Wdown_s.at((long)si * f * d), d, 0), g, sp, st));
+          gemm_run(EPI_GELU_BWD, opnd(ln.dy16, d, 0), opnd(c->Wdown_s.at((long)si * f * d), d, 0), g, sp, st));
       GemmArgs g2;
       g2.M = n; g2.N = d; g2.K = f;
-      g2.out32 = c->dxn; g2.ldo32 = d; g2.resid = c->dxn; g2.ldr = d; g2.err = c->derr; g2.allow_ksplit = true;
+      g2.out32 = ln.dxn; g2.ldo32 = d; g2.resid = ln.dxn; g2.ldr = d; g2.err = c->derr; g2.allow_ksplit = true;
       RUN(K_MLP_DX, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 0,
-          gemm_run(EPI_RESID, opnd(c->da_s, f, 0), opnd(c->Wup_s.at((long)si * d * f), f, 0), g2, sp, st));
+          gemm_run(EPI_RESID, opnd(ln.da_s, f, 0), opnd(c->Wup_s.at((long)si * d * f), f, 0), g2, sp, st));
     }
     {  // W_up -= eta Xn_m^T dA
       if (side) {
-        CK(cudaEventRecord(c->ev_dx, st));
-        CK(cudaStreamWaitEvent(sw, c->ev_dx, 0));
+        CK(cudaEventRecord(ln.ev_dx, st));
+        CK(cudaStreamWaitEvent(sw, ln.ev_dx, 0));
       }
       GemmArgs g;
       g.M = d; g.N = f; g.K = n;
       g.w32 = sq_.up32 + (long)si * d * f; g.wh = up16.hi; g.wl = up16.lo; g.ldw = f; g.eta = eta;
       g.err = c->derr;
       RUN_ON(sw, K_DW_SGD, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 8 * dd * ff,
-             gemm_run(EPI_SGD, opnd(c->sxm.at((long)si * b * d), d, 1), opnd(c->da, f, 1), g, sp, sw));
+             gemm_run(EPI_SGD, opnd(ln.sxm.at((long)si * b * d), d, 1), opnd(ln.da, f, 1), g, sp, sw));
       if (side) {
-        CK(cudaEventRecord(c->ev_wu, sw));
+        CK(cudaEventRecord(ln.ev_wu, sw));
         wu_pending = true;
       }
     }
     if (si == 0) break;  // the first trainable block's attention needs no gradient
     // dH = dY + RMSNorm_m^T(dXn_m)
     RUN(K_RMSNORM, 1, 0, 0, nn * dd * (20 + eb),
-        rows_rmsnorm_bwd(c->dxn, c->sh + (long)si * b * d, c->gains + (long)(2 * l + 1) * d,
-                         c->srs_m + (long)si * b, c->dy, n, d, c->dh32, c->dh16.hi, c->dh16.lo, st));
+        rows_rmsnorm_bwd(ln.dxn, ln.sh + (long)si * b * d, c->gains + (long)(2 * l + 1) * d,
+                         ln.srs_m + (long)si * b, ln.dy, n, d, ln.dh32, ln.dh16.hi, ln.dh16.lo, st));
     {  // dO = dH Wo^T
       GemmArgs g;
       g.M = n; g.N = d; g.K = d;
-      g.oh = c->do16.hi; g.ol = c->do16.lo; g.ldo = d; g.err = c->derr;
+      g.oh = ln.do16.hi; g.ol = ln.do16.lo; g.ldo = d; g.err = c->derr;
       RUN(K_ATTN_DX, 1, 2 * nn * dd * dd, 2 * nn * dd * dd * ops, 0,
-          gemm_run(EPI_OPND, opnd(c->dh16, d, 0), opnd(c->Wo.at((long)l * d * d), d, 0), g, sp, st));
+          gemm_run(EPI_OPND, opnd(ln.dh16, d, 0), opnd(c->Wo.at((long)l * d * d), d, 0), g, sp, st));
     }
-    Pair qb = c->sq.at((long)si * b * d), ob = c->so.at((long)si * b * d);
+    Pair qb = ln.sq.at((long)si * b * d), ob = ln.so.at((long)si * b * d);
     RUN(K_MISC, 1, 0, 0, nn * dd * 2 * eb,
-        rows_attn_rowdot(c->do16.hi, c->do16.lo, ob.hi, ob.lo, n, H, dh, c->D, st));
+        rows_attn_rowdot(ln.do16.hi, ln.do16.lo, ob.hi, ob.lo, n, H, dh, ln.D, st));
     {
       AttnBwdMaps m;
-      Pair ko = c->kown.at((long)l * R * d), vo = c->vown.at((long)l * R * d);
+      Pair ko = ln.kown.at((long)l * R * d), vo = ln.vown.at((long)l * R * d);
       Pair kr = sq_.ring_k.at((long)l * k * d), vr = sq_.ring_v.at((long)l * k * d);
       if (!attn_maps(&m.f, qb, kr, vr, ko, vo, n, d, k) ||
-          !make_map(&m.dO, c->do16.hi, (uint64_t)d, (uint64_t)n, d, 128))
+          !make_map(&m.dO, ln.do16.hi, (uint64_t)d, (uint64_t)n, d, 128))
         return fail(c, TTT_ERR_CUDA, "attention backward tensor maps");
       if (sp) {
-        if (!make_map(&m.dOl, c->do16.lo, (uint64_t)d, (uint64_t)n, d, 128))
+        if (!make_map(&m.dOl, ln.do16.lo, (uint64_t)d, (uint64_t)n, d, 128))
           return fail(c, TTT_ERR_CUDA, "attention backward tensor maps");
       } else {
         m.dOl = m.dO;
@@ -562,11 +578,11 @@ int suffix_step(ttt_ctx* c, int s, int row, const int* tok, int n, const int* ne
       ba.g.n = n; ba.g.H = H; ba.g.dh = dh; ba.g.window = k; ba.g.pos0 = pos0;
       ba.g.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)dh));
       ba.g.ldo = d; ba.g.err = c->derr;
-      ba.lse = c->slse + (long)si * H * b;
-      ba.D = c->D;
+      ba.lse = ln.slse + (long)si * H * b;
+      ba.D = ln.D;
       ba.scale = (float)(1.0 / std::sqrt((double)dh));
       // written straight into the QKV dX product's operand, RoPE's rotation transposed
-      ba.qkv_h = c->dqkv.hi; ba.qkv_l = c->dqkv.lo; ba.ld_qkv = 3L * d; ba.k_off = d; ba.v_off = 2L * d;
+      ba.qkv_h = ln.dqkv.hi; ba.qkv_l = ln.dqkv.lo; ba.ld_qkv = 3L * d; ba.k_off = d; ba.v_off = 2L * d;
       ba.cs = cs; ba.sn = sn;
       RUN(K_ATTN_BWD, 1, 4 * dd * (pairs + own_pairs), (6 * dd * tpairs + 8 * dd * own_tile_pairs) * ops, 0,
           attn_bwd_run(m, ba, sp, st, 0));
@@ -574,35 +590,35 @@ int suffix_step(ttt_ctx* c, int s, int row, const int* tok, int n, const int* ne
     {  // dXn_a = dQKV Wqkv^T
       GemmArgs g;
       g.M = n; g.N = d; g.K = 3 * d;
-      g.out32 = c->dxn; g.ldo32 = d; g.err = c->derr; g.allow_ksplit = true;
+      g.out32 = ln.dxn; g.ldo32 = d; g.err = c->derr; g.allow_ksplit = true;
       RUN(K_ATTN_DX, 1, 6 * nn * dd * dd, 6 * nn * dd * dd * ops, 0,
-          gemm_run(EPI_F32, opnd(c->dqkv, 3 * d, 0), opnd(c->Wqkv.at((long)l * d * 3 * d), 3 * d, 0), g, sp, st));
+          gemm_run(EPI_F32, opnd(ln.dqkv, 3 * d, 0), opnd(c->Wqkv.at((long)l * d * 3 * d), 3 * d, 0), g, sp, st));
     }
     if (wd_pending) {  // the W_down step has read dY
-      CK(cudaStreamWaitEvent(st, c->ev_wd, 0));
+      CK(cudaStreamWaitEvent(st, ln.ev_wd, 0));
       wd_pending = false;
     }
     // dY_{l-1} = dH + RMSNorm_a^T(dXn_a)
     RUN(K_RMSNORM, 1, 0, 0, nn * dd * (20 + eb),
-        rows_rmsnorm_bwd(c->dxn, c->sx + (long)si * b * d, c->gains + (long)(2 * l) * d, c->srs_a + (long)si * b,
-                         c->dh32, n, d, c->dy, c->dy16.hi, c->dy16.lo, st));
+        rows_rmsnorm_bwd(ln.dxn, ln.sx + (long)si * b * d, c->gains + (long)(2 * l) * d, ln.srs_a + (long)si * b,
+                         ln.dh32, n, d, ln.dy, ln.dy16.hi, ln.dy16.lo, st));
   }
   if (side) {  // every step of this chunk is in place before anything later reads the weights
-    CK(cudaStreamWaitEvent(st, c->ev_wd, 0));
-    CK(cudaStreamWaitEvent(st, c->ev_wu, 0));
+    CK(cudaStreamWaitEvent(st, ln.ev_wd, 0));
+    CK(cudaStreamWaitEvent(st, ln.ev_wu, 0));
   }
   // ------------------------------------------------------------------- commit
   const double cb = (double)S * nn * dd * 2 * 2;
   const long os = (long)R * d, rs = (long)k * d;
   RUN(K_COMMIT, 1, 0, 0, cb,
-      rows_commit(c->kown.hi + (long)P0 * os, sq_.ring_k.hi + (long)P0 * rs, os, rs, S, pos0, n, k, d, st));
+      rows_commit(ln.kown.hi + (long)P0 * os, sq_.ring_k.hi + (long)P0 * rs, os, rs, S, pos0, n, k, d, st));
   RUN(K_COMMIT, 1, 0, 0, cb,
-      rows_commit(c->vown.hi + (long)P0 * os, sq_.ring_v.hi + (long)P0 * rs, os, rs, S, pos0, n, k, d, st));
+      rows_commit(ln.vown.hi + (long)P0 * os, sq_.ring_v.hi + (long)P0 * rs, os, rs, S, pos0, n, k, d, st));
   if (sp) {
     RUN(K_COMMIT, 1, 0, 0, cb,
-        rows_commit(c->kown.lo + (long)P0 * os, sq_.ring_k.lo + (long)P0 * rs, os, rs, S, pos0, n, k, d, st));
+        rows_commit(ln.kown.lo + (long)P0 * os, sq_.ring_k.lo + (long)P0 * rs, os, rs, S, pos0, n, k, d, st));
     RUN(K_COMMIT, 1, 0, 0, cb,
-        rows_commit(c->vown.lo + (long)P0 * os, sq_.ring_v.lo + (long)P0 * rs, os, rs, S, pos0, n, k, d, st));
+        rows_commit(ln.vown.lo + (long)P0 * os, sq_.ring_v.lo + (long)P0 * rs, os, rs, S, pos0, n, k, d, st));
   }
   sq_.pos = pos0 + n;
   return TTT_OK;
@@ -660,79 +676,88 @@ extern "C" int ttt_create(const ttt_config* cfg, void* cuda_stream, ttt_ctx** ou
   c->init_down = dalloc<float>(c, S * f * d, ok);
   c->acc.resize(K_NCLS);
   c->tok = dalloc<int>(c, (size_t)g.n_seqs * b, ok);
-  c->tgt = dalloc<int>(c, b, ok);
   c->next = dalloc<int>(c, g.n_seqs, ok);
   c->minus1 = dalloc<int>(c, 1, ok);
   c->derr = dalloc<int>(c, 1, ok);
   c->loss_dev = dalloc<float>(c, g.n_seqs, ok);
   c->inv_freq = dalloc<double>(c, dh / 2, ok);
-  const long R = c->R;
-  c->cs = dalloc<float>(c, R * dh / 2, ok);
-  c->sn = dalloc<float>(c, R * dh / 2, ok);
-  c->x = dalloc<float>(c, b * d, ok);
-  c->xp = dalloc<float>(c, R * d, ok);
-  c->xpb[0] = c->xp;
-  c->xpb[1] = dalloc<float>(c, R * d, ok);
-  c->csb[0] = c->cs;
-  c->snb[0] = c->sn;
-  c->csb[1] = dalloc<float>(c, R * dh / 2, ok);
-  c->snb[1] = dalloc<float>(c, R * dh / 2, ok);
-  c->sxn = palloc(c, b * d, ok);
-  c->qkv = dalloc<float>(c, R * 3 * d, ok);
-  c->xn = palloc(c, R * d, ok);
-  c->q = palloc(c, R * d, ok);
-  c->o = palloc(c, R * d, ok);
-  c->u = palloc(c, R * f, ok);
-  c->kown = palloc(c, L * R * d, ok);
-  c->vown = palloc(c, L * R * d, ok);
-  c->sx = dalloc<float>(c, S * b * d, ok);
-  c->sh = dalloc<float>(c, S * b * d, ok);
-  c->srs_a = dalloc<float>(c, S * b, ok);
-  c->srs_m = dalloc<float>(c, S * b, ok);
-  c->slse = dalloc<float>(c, S * H * b, ok);
-  c->sa = dalloc<float>(c, S * b * f, ok);
-  c->sq = palloc(c, S * b * d, ok);
-  c->so = palloc(c, S * b * d, ok);
-  c->sxm = palloc(c, S * b * d, ok);
-  c->su = palloc(c, S * b * f, ok);
-  c->xf = palloc(c, b * d, ok);
-  c->dz = palloc(c, b * V, ok);
-  c->rs_f = dalloc<float>(c, b, ok);
-  c->zt = dalloc<float>(c, b, ok);
-  c->lse_row = dalloc<float>(c, b, ok);
-  c->loss_row = dalloc<float>(c, b, ok);
-  c->inv_nvalid = dalloc<float>(c, 1, ok);
-  c->part = dalloc<float2>(c, ((V + 127) / 128) * b, ok);
-  c->dy = dalloc<float>(c, b * d, ok);
-  c->dxn = dalloc<float>(c, b * d, ok);
-  c->dh32 = dalloc<float>(c, b * d, ok);
-  c->D = dalloc<float>(c, H * b, ok);
-  c->dy16 = palloc(c, b * d, ok);
-  c->da = palloc(c, b * f, ok);
-  c->dh16 = palloc(c, b * d, ok);
-  c->do16 = palloc(c, b * d, ok);
-  c->dqkv = palloc(c, b * 3 * d, ok);
   c->zdec = dalloc<float>(c, V, ok);
-  if (c->dual) {
-    c->sa_s = dalloc<float>(c, S * b * f, ok);
-    c->us = palloc(c, b * f, ok);
-    c->da_s = palloc(c, b * f, ok);
+  const long R = c->R;
+  const bool fused_qkv = qkv_rope_bn(dh, (int)d, split) != 0;
+  c->lanes.resize(std::min(g.n_seqs, kMaxLanes));
+  for (Lane& ln : c->lanes) {
+    ln.tgt = dalloc<int>(c, b, ok);
+    ln.cs = dalloc<float>(c, R * dh / 2, ok);
+    ln.sn = dalloc<float>(c, R * dh / 2, ok);
+    ln.x = dalloc<float>(c, b * d, ok);
+    ln.xp = dalloc<float>(c, R * d, ok);
+    ln.xpb[0] = ln.xp;
+    ln.xpb[1] = dalloc<float>(c, R * d, ok);
+    ln.csb[0] = ln.cs;
+    ln.snb[0] = ln.sn;
+    ln.csb[1] = dalloc<float>(c, R * dh / 2, ok);
+    ln.snb[1] = dalloc<float>(c, R * dh / 2, ok);
+    ln.sxn = palloc(c, b * d, ok);
+    if (!fused_qkv) ln.qkv = dalloc<float>(c, R * 3 * d, ok);
+    ln.xn = palloc(c, R * d, ok);
+    ln.q = palloc(c, R * d, ok);
+    ln.o = palloc(c, R * d, ok);
+    ln.u = palloc(c, R * f, ok);
+    ln.kown = palloc(c, L * R * d, ok);
+    ln.vown = palloc(c, L * R * d, ok);
+    ln.sx = dalloc<float>(c, S * b * d, ok);
+    ln.sh = dalloc<float>(c, S * b * d, ok);
+    ln.srs_a = dalloc<float>(c, S * b, ok);
+    ln.srs_m = dalloc<float>(c, S * b, ok);
+    ln.slse = dalloc<float>(c, S * H * b, ok);
+    ln.sa = dalloc<float>(c, S * b * f, ok);
+    ln.sq = palloc(c, S * b * d, ok);
+    ln.so = palloc(c, S * b * d, ok);
+    ln.sxm = palloc(c, S * b * d, ok);
+    ln.su = palloc(c, S * b * f, ok);
+    ln.xf = palloc(c, b * d, ok);
+    ln.dz = palloc(c, b * V, ok);
+    ln.rs_f = dalloc<float>(c, b, ok);
+    ln.zt = dalloc<float>(c, b, ok);
+    ln.lse_row = dalloc<float>(c, b, ok);
+    ln.loss_row = dalloc<float>(c, b, ok);
+    ln.inv_nvalid = dalloc<float>(c, 1, ok);
+    ln.part = dalloc<float2>(c, ((V + 127) / 128) * b, ok);
+    ln.dy = dalloc<float>(c, b * d, ok);
+    ln.dxn = dalloc<float>(c, b * d, ok);
+    ln.dh32 = dalloc<float>(c, b * d, ok);
+    ln.D = dalloc<float>(c, H * b, ok);
+    ln.dy16 = palloc(c, b * d, ok);
+    ln.da = palloc(c, b * f, ok);
+    ln.dh16 = palloc(c, b * d, ok);
+    ln.do16 = palloc(c, b * d, ok);
+    ln.dqkv = palloc(c, b * 3 * d, ok);
+    if (c->dual) {
+      ln.sa_s = dalloc<float>(c, S * b * f, ok);
+      ln.us = palloc(c, b * f, ok);
+      ln.da_s = palloc(c, b * f, ok);
+    }
   }
   if (!ok) {
     ttt_destroy(c);
     return TTT_ERR_OOM;
   }
-  if (cudaStreamCreateWithFlags(&c->st2, cudaStreamNonBlocking) != cudaSuccess ||
-      cudaStreamCreateWithFlags(&c->st3, cudaStreamNonBlocking) != cudaSuccess ||
-      cudaEventCreateWithFlags(&c->ev_da, cudaEventDisableTiming) != cudaSuccess ||
-      cudaEventCreateWithFlags(&c->ev_dx, cudaEventDisableTiming) != cudaSuccess ||
-      cudaEventCreateWithFlags(&c->ev_wd, cudaEventDisableTiming) != cudaSuccess ||
-      cudaEventCreateWithFlags(&c->ev_wu, cudaEventDisableTiming) != cudaSuccess ||
-      cudaEventCreateWithFlags(&c->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
-      cudaEventCreateWithFlags(&c->ev_pass[0], cudaEventDisableTiming) != cudaSuccess ||
-      cudaEventCreateWithFlags(&c->ev_pass[1], cudaEventDisableTiming) != cudaSuccess ||
-      cudaEventCreateWithFlags(&c->ev_suf[0], cudaEventDisableTiming) != cudaSuccess ||
-      cudaEventCreateWithFlags(&c->ev_suf[1], cudaEventDisableTiming) != cudaSuccess) {
+  auto mk_ev = [](cudaEvent_t* e) { return cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess; };
+  auto mk_st = [](cudaStream_t* t) { return cudaStreamCreateWithFlags(t, cudaStreamNonBlocking) == cudaSuccess; };
+  bool made = mk_ev(&c->ev_fork);
+  for (size_t i = 0; i < c->lanes.size() && made; ++i) {
+    Lane& ln = c->lanes[i];
+    if (i == 0) {
+      ln.st = c->st;
+    } else {
+      made = mk_st(&ln.st);
+      ln.own_st = made;
+    }
+    made = made && mk_st(&ln.st2) && mk_st(&ln.st3) && mk_ev(&ln.ev_da) && mk_ev(&ln.ev_dx) && mk_ev(&ln.ev_wd) &&
+           mk_ev(&ln.ev_wu) && mk_ev(&ln.ev_fork) && mk_ev(&ln.ev_join) && mk_ev(&ln.ev_pass[0]) &&
+           mk_ev(&ln.ev_pass[1]) && mk_ev(&ln.ev_suf[0]) && mk_ev(&ln.ev_suf[1]);
+  }
+  if (!made) {
     cudaGetLastError();
     ttt_destroy(c);
     return TTT_ERR_CUDA;
@@ -753,14 +778,18 @@ extern "C" int ttt_create(const ttt_config* cfg, void* cuda_stream, ttt_ctx** ou
 extern "C" void ttt_destroy(ttt_ctx* c) {
   if (!c) return;
   if (c->st) cudaStreamSynchronize(c->st);
-  if (c->st2) cudaStreamSynchronize(c->st2);
-  if (c->st3) cudaStreamSynchronize(c->st3);
+  for (Lane& ln : c->lanes)
+    for (cudaStream_t t : {ln.own_st ? ln.st : nullptr, ln.st2, ln.st3})
+      if (t) cudaStreamSynchronize(t);
   cudaDeviceSynchronize();
-  if (c->st2) cudaStreamDestroy(c->st2);
-  if (c->st3) cudaStreamDestroy(c->st3);
-  for (cudaEvent_t e : {c->ev_fork, c->ev_pass[0], c->ev_pass[1], c->ev_suf[0], c->ev_suf[1], c->ev_da, c->ev_dx,
-                        c->ev_wd, c->ev_wu})
-    if (e) cudaEventDestroy(e);
+  for (Lane& ln : c->lanes) {
+    for (cudaStream_t t : {ln.own_st ? ln.st : nullptr, ln.st2, ln.st3})
+      if (t) cudaStreamDestroy(t);
+    for (cudaEvent_t e : {ln.ev_fork, ln.ev_join, ln.ev_pass[0], ln.ev_pass[1], ln.ev_suf[0], ln.ev_suf[1], ln.ev_da,
+                          ln.ev_dx, ln.ev_wd, ln.ev_wu})
+      if (e) cudaEventDestroy(e);
+  }
+  if (c->ev_fork) cudaEventDestroy(c->ev_fork);
   for (void* p : c->allocs) cudaFree(p);
   if (c->seq_tok) cudaFree(c->seq_tok);
   if (c->seq_loss) cudaFree(c->seq_loss);
@@ -878,16 +907,56 @@ extern "C" int ttt_sync(ttt_ctx* c) {
   return check_device_error(c);
 }
 
+namespace {
+// Lanes 0 .. nl-1, side streams included, start after everything already enqueued
+// on the context stream.
+int fork_lanes(ttt_ctx* c, int nl) {
+  CK(cudaEventRecord(c->ev_fork, c->st));
+  for (int i = 0; i < nl; ++i) {
+    Lane& ln = c->lanes[i];
+    if (ln.own_st) CK(cudaStreamWaitEvent(ln.st, c->ev_fork, 0));
+    CK(cudaStreamWaitEvent(ln.st2, c->ev_fork, 0));
+    CK(cudaStreamWaitEvent(ln.st3, c->ev_fork, 0));
+  }
+  return TTT_OK;
+}
+
+// The context stream waits for everything lanes 0 .. nl-1 enqueued on any of their streams.
+int join_lanes(ttt_ctx* c, int nl) {
+  for (int i = 0; i < nl; ++i) {
+    Lane& ln = c->lanes[i];
+    for (cudaStream_t t : {ln.st2, ln.st3, ln.own_st ? ln.st : nullptr}) {
+      if (!t) continue;
+      CK(cudaEventRecord(ln.ev_join, t));
+      CK(cudaStreamWaitEvent(c->st, ln.ev_join, 0));
+    }
+  }
+  return TTT_OK;
+}
+
+// Lanes side by side when concurrency is on, else one lane for every sequence in turn.
+int lanes_in_use(const ttt_ctx* c) { return c->concurrent ? (int)c->lanes.size() : 1; }
+}  // namespace
+
 extern "C" int ttt_prefill_chunk_dev(ttt_ctx* c, const int32_t* d_tokens, int32_t n, const int32_t* d_next,
                                      float* d_loss) {
   if (!c || !d_tokens || !d_next || !d_loss) return TTT_ERR_ARG;
   if (!c->loaded) return fail(c, TTT_ERR_STATE, "weights not loaded");
   if (n < 1 || n > c->b) return fail(c, TTT_ERR_ARG, "n outside 1..chunk");
-  for (int s = 0; s < c->B; ++s) {
-    const int32_t* tk = d_tokens + (long)s * n;
-    int r = prefix_pass(c, s, tk, n, c->seqs[s].pos, c->st, 0);
-    if (r == TTT_OK) r = suffix_step(c, s, 0, tk, n, d_next + s, d_loss + s);
+  const int nl = lanes_in_use(c);
+  for (int s0 = 0; s0 < c->B; s0 += nl) {
+    const int m = std::min(nl, c->B - s0);
+    int r = fork_lanes(c, m);
+    for (int i = 0; i < m && r == TTT_OK; ++i) {
+      Lane& ln = c->lanes[i];
+      const int s = s0 + i;
+      const int32_t* tk = d_tokens + (long)s * n;
+      r = prefix_pass(c, ln, s, tk, n, c->seqs[s].pos, ln.st, 0);
+      if (r == TTT_OK) r = suffix_step(c, ln, s, 0, tk, n, d_next + s, d_loss + s);
+    }
+    const int rj = join_lanes(c, m);
     if (r != TTT_OK) return r;
+    if (rj != TTT_OK) return rj;
   }
   return TTT_OK;
 }
@@ -913,73 +982,77 @@ extern "C" int ttt_prefill_chunk(ttt_ctx* c, const int32_t* tokens, int32_t n, c
 }
 
 namespace {
-// Sequence s over T tokens (device ids): the frozen blocks run ahead over groups of
-// G chunks, the trainable blocks step chunk by chunk; losses[ceil(T/b)] (device).
-// With more than one group, the frozen pass of group g+1 runs on the second stream
-// while group g's trainable steps run on the context stream: the pass outputs are
-// double-buffered, the steps of group g wait for pass g, and pass g+2 waits for the
-// steps of group g (the last readers of its buffer).  The two sides share no other
-// buffer: the steps touch only the trainable blocks' keys/values and window caches.
-int prefill_one(ttt_ctx* c, int s, const int32_t* seq, int T, float* losses) {
+// Sequences s0 .. s0+nl-1 over T tokens each (device ids toks[B][T]), sequence
+// s0+i on lane i: the frozen blocks run ahead over groups of G chunks, the
+// trainable blocks step chunk by chunk; losses[B][ceil(T/b)] (device).  With
+// more than one group, the frozen pass of group g+1 runs on the lane's second
+// stream while group g's trainable steps run on its main stream: the pass
+// outputs are double-buffered, the steps of group g wait for pass g, and pass
+// g+2 waits for the steps of group g (the last readers of its buffer).  The two
+// sides share no other buffer: the steps touch only the trainable blocks'
+// keys/values and window caches.  The lanes' work is enqueued chunk by chunk in
+// turn, so every lane has launches queued while the others run.
+int prefill_lanes(ttt_ctx* c, int s0, int nl, const int32_t* toks, int T, float* losses) {
   const int b = c->b, G = c->G;
   const int nc = (T + b - 1) / b, ng = (nc + G - 1) / G;
-  const long base = c->seqs[s].pos;
-  auto steps = [&](int g, int buf) -> int {
-    const int g0 = g * G, g1 = std::min(nc, g0 + G), t0 = g0 * b;
-    for (int ci = g0; ci < g1; ++ci) {
-      const int s0 = ci * b, n = std::min(b, T - s0);
-      const int32_t* nx = (s0 + n < T) ? seq + s0 + n : c->minus1;
-      const int r = suffix_step(c, s, s0 - t0, seq + s0, n, nx, losses + ci, buf);
-      if (r != TTT_OK) return r;
-    }
-    return TTT_OK;
-  };
-  auto pass = [&](int g, cudaStream_t st, int buf) -> int {
-    const int t0 = g * G * b, t1 = std::min(T, (g + 1) * G * b);
-    return prefix_pass(c, s, seq + t0, t1 - t0, base + t0, st, buf);
-  };
   const bool overlap = ng > 1 && c->concurrent && qkv_rope_bn(c->dh, c->d, c->split) != 0;
-  if (!overlap) {
-    for (int g = 0; g < ng; ++g) {
-      int r = pass(g, c->st, 0);
-      if (r == TTT_OK) r = steps(g, 0);
-      if (r != TTT_OK) return r;
-    }
-    return TTT_OK;
-  }
-  // the second stream starts after everything already enqueued on the context stream
-  CK(cudaEventRecord(c->ev_fork, c->st));
-  CK(cudaStreamWaitEvent(c->st2, c->ev_fork, 0));
-  auto ahead = [&](int g) -> int {
-    if (g >= 2) CK(cudaStreamWaitEvent(c->st2, c->ev_suf[g & 1], 0));
-    const int r = pass(g, c->st2, g & 1);
+  std::vector<long> base(nl);
+  for (int i = 0; i < nl; ++i) base[i] = c->seqs[s0 + i].pos;
+  auto seq = [&](int i) { return toks + (long)(s0 + i) * T; };
+  auto pass = [&](int i, int g, cudaStream_t st, int buf) -> int {
+    const int t0 = g * G * b, t1 = std::min(T, (g + 1) * G * b);
+    return prefix_pass(c, c->lanes[i], s0 + i, seq(i) + t0, t1 - t0, base[i] + t0, st, buf);
+  };
+  auto ahead = [&](int i, int g) -> int {
+    Lane& ln = c->lanes[i];
+    if (g >= 2) CK(cudaStreamWaitEvent(ln.st2, ln.ev_suf[g & 1], 0));
+    const int r = pass(i, g, ln.st2, g & 1);
     if (r != TTT_OK) return r;
-    CK(cudaEventRecord(c->ev_pass[g & 1], c->st2));
+    CK(cudaEventRecord(ln.ev_pass[g & 1], ln.st2));
     return TTT_OK;
   };
-  int r = ahead(0);
-  for (int g = 0; g < ng && r == TTT_OK; ++g) {
-    if (g + 1 < ng) r = ahead(g + 1);
-    if (r != TTT_OK) break;
-    CK(cudaStreamWaitEvent(c->st, c->ev_pass[g & 1], 0));
-    r = steps(g, g & 1);
-    if (r != TTT_OK) break;
-    CK(cudaEventRecord(c->ev_suf[g & 1], c->st));
-  }
-  if (r != TTT_OK) {  // keep later work on the context stream behind whatever the second stream has queued
-    cudaEventRecord(c->ev_fork, c->st2);
-    cudaStreamWaitEvent(c->st, c->ev_fork, 0);
-  }
-  return r;
+  auto body = [&]() -> int {
+    if (overlap)
+      for (int i = 0; i < nl; ++i) {
+        const int r = ahead(i, 0);
+        if (r != TTT_OK) return r;
+      }
+    for (int g = 0; g < ng; ++g) {
+      for (int i = 0; i < nl; ++i) {
+        Lane& ln = c->lanes[i];
+        const int r = !overlap ? pass(i, g, ln.st, 0) : (g + 1 < ng ? ahead(i, g + 1) : TTT_OK);
+        if (r != TTT_OK) return r;
+        if (overlap) CK(cudaStreamWaitEvent(ln.st, ln.ev_pass[g & 1], 0));
+      }
+      const int g0 = g * G, g1 = std::min(nc, g0 + G), t0 = g0 * b;
+      for (int ci = g0; ci < g1; ++ci) {
+        const int p0 = ci * b, n = std::min(b, T - p0);
+        for (int i = 0; i < nl; ++i) {
+          const int32_t* sq = seq(i);
+          const int32_t* nx = (p0 + n < T) ? sq + p0 + n : c->minus1;
+          const int r = suffix_step(c, c->lanes[i], s0 + i, p0 - t0, sq + p0, n, nx,
+                                    losses + (long)(s0 + i) * nc + ci, overlap ? (g & 1) : 0);
+          if (r != TTT_OK) return r;
+        }
+      }
+      if (overlap)
+        for (int i = 0; i < nl; ++i) CK(cudaEventRecord(c->lanes[i].ev_suf[g & 1], c->lanes[i].st));
+    }
+    return TTT_OK;
+  };
+  int r = fork_lanes(c, nl);
+  if (r == TTT_OK) r = body();
+  const int rj = join_lanes(c, nl);  // also on failure: later work stays behind what was queued
+  return r != TTT_OK ? r : rj;
 }
 }  // namespace
 
 extern "C" int ttt_prefill_sequence_dev(ttt_ctx* c, const int32_t* d_tokens, int32_t T, float* d_losses) {
   if (!c || !d_tokens || !d_losses || T < 1) return TTT_ERR_ARG;
   if (!c->loaded) return fail(c, TTT_ERR_STATE, "weights not loaded");
-  const int nc = (T + c->b - 1) / c->b;
-  for (int s = 0; s < c->B; ++s) {
-    const int r = prefill_one(c, s, d_tokens + (long)s * T, T, d_losses + (long)s * nc);
+  const int nl = lanes_in_use(c);
+  for (int s0 = 0; s0 < c->B; s0 += nl) {
+    const int r = prefill_lanes(c, s0, std::min(nl, c->B - s0), d_tokens, T, d_losses);
     if (r != TTT_OK) return r;
   }
   return TTT_OK;
@@ -1005,39 +1078,39 @@ extern "C" int ttt_decode_dev(ttt_ctx* c, const int32_t* d_prompt, int32_t T, in
   if ((sample != 0 && sample != 1) || (sample && (!d_u || !(temp > 0.f)))) return TTT_ERR_ARG;
   if (n_new >= c->b && !d_gen_losses) return TTT_ERR_ARG;
   if (!c->loaded) return fail(c, TTT_ERR_STATE, "weights not loaded");
-  cudaStream_t st = c->st;
+  Lane& ln = c->lanes[0];  // decoding runs every sequence on the first lane in turn
+  cudaStream_t st = ln.st;
   const int b = c->b, L = c->L, P0 = c->L - c->S, d = c->d, dh = c->dh, V = c->V;
   const int ncp = (T + b - 1) / b, ncg = n_new / b;
   const double dd = d;
   for (int s = 0; s < c->B; ++s) {
     Seq& sq_ = c->seqs[s];
-    const int32_t* prompt = d_prompt + (long)s * T;
     int32_t* out = d_out + (long)s * (n_new + 1);
     const float* u = d_u ? d_u + (long)s * (n_new + 1) : nullptr;
     auto zrow = [&](int i) { return d_logits ? d_logits + ((long)s * (n_new + 1) + i) * V : c->zdec; };
     // the prompt goes through the chunked inner loop; its last position has no target
-    int r = prefill_one(c, s, prompt, T, d_prefill_losses + (long)s * ncp);
+    int r = prefill_lanes(c, s, 1, d_prompt, T, d_prefill_losses);
     if (r != TTT_OK) return r;
     // the first token comes from the prompt's last position, as the last prompt chunk's
     // forward computed it (before that chunk's update): the final hidden rows are still in xf
     const int nl = T - (ncp - 1) * b;
-    r = logits_row(c, c->xf.at((long)(nl - 1) * d), zrow(0));
+    r = logits_row(c, ln.xf.at((long)(nl - 1) * d), zrow(0));
     if (r != TTT_OK) return r;
     RUN(K_MISC, 1, 0, 0, (double)V * 4, rows_pick(zrow(0), V, sample, temp, u, out, st));
     for (int i = 0; i < n_new; ++i) {
       const int rr = i % b;           // row of the token in its generated chunk
       const long pos0 = sq_.pos;      // first position of that chunk
-      if (rr == 0) RUN(K_ROPE, 1, 0, 0, (double)b * dh * 4, rows_rope_table(pos0, b, dh, c->inv_freq, c->cs, c->sn, st));
+      if (rr == 0) RUN(K_ROPE, 1, 0, 0, (double)b * dh * 4, rows_rope_table(pos0, b, dh, c->inv_freq, ln.cs, ln.sn, st));
       // one-token forward with the chunk's starting fast weights; its keys/values go to row
       // rr of the chunk's own buffers, the window cache is untouched until the chunk's step
-      float* x = c->xp + (long)rr * d;
+      float* x = ln.xp + (long)rr * d;
       RUN(K_MISC, 1, 0, 0, dd * 8, rows_embed(out + i, 1, c->E, V, d, x, c->derr, st));
       for (int l = 0; l < L; ++l) {
-        r = layer_forward(c, sq_, l, l >= P0 ? l - P0 : -1, false, 1, rr, pos0, x, x, c->cs + (long)rr * (dh / 2),
-                          c->sn + (long)rr * (dh / 2), st);
+        r = layer_forward(c, ln, sq_, l, l >= P0 ? l - P0 : -1, false, 1, rr, pos0, x, x, ln.cs + (long)rr * (dh / 2),
+                          ln.sn + (long)rr * (dh / 2), st);
         if (r != TTT_OK) return r;
       }
-      Pair xf = c->xf.at((long)rr * d);
+      Pair xf = ln.xf.at((long)rr * d);
       RUN(K_RMSNORM, 1, 0, 0, dd * 8,
           rows_rmsnorm(x, c->gains + (long)(2 * L) * d, c->cfg.rms_eps, 1, d, xf.hi, xf.lo, nullptr, st));
       r = logits_row(c, xf, zrow(i + 1));
@@ -1045,8 +1118,8 @@ extern "C" int ttt_decode_dev(ttt_ctx* c, const int32_t* d_prompt, int32_t T, in
       RUN(K_MISC, 1, 0, 0, (double)V * 4, rows_pick(zrow(i + 1), V, sample, temp, u ? u + i + 1 : nullptr, out + i + 1, st));
       if (rr == b - 1) {  // a complete generated chunk takes one inner-loop step; its last target is the pick above
         const int32_t* ids = out + i - (b - 1);
-        r = prefix_pass(c, s, ids, b, pos0, c->st, 0);
-        if (r == TTT_OK) r = suffix_step(c, s, 0, ids, b, out + i + 1, d_gen_losses + (long)s * ncg + i / b);
+        r = prefix_pass(c, ln, s, ids, b, pos0, st, 0);
+        if (r == TTT_OK) r = suffix_step(c, ln, s, 0, ids, b, out + i + 1, d_gen_losses + (long)s * ncg + i / b);
         if (r != TTT_OK) return r;
       }
     }

@@ -245,3 +245,62 @@ def test_state_import_rejects_another_shape():
         m.import_state(state + bytes(int(T.ttt_state_bytes(m._h)) - len(state)), 0)
     assert e.value.code == T.TTT_ERR_ARG
     m.close()
+
+
+# ------------------------------------------------------------------ several sequences per context
+def multi_sequence_case(name, n_seqs):
+    s = SMALL[name].replace(n_seqs=n_seqs)
+    toks = np.stack([zipf_tokens(s.seq_len, s.vocab, seed=2000 + q) for q in range(n_seqs)]).astype(np.int32)
+    return s, toks
+
+
+def run_gpu_multi(shape, toks, blob, api, concurrent):
+    B, Tn, b = toks.shape[0], toks.shape[1], shape.chunk
+    nc = -(-Tn // b)
+    m = T.TTT.from_shape(shape)
+    try:
+        m.load_weights(blob)
+        m.set_concurrency(concurrent)
+        if api == "sequence":
+            d_tok = torch.tensor(toks, device="cuda")
+            d_loss = torch.zeros((B, nc), dtype=torch.float32, device="cuda")
+            m.prefill_sequence_dev(d_tok, Tn, d_loss)
+            m.sync()
+            losses = d_loss.cpu().numpy().astype(np.float64)
+        else:
+            losses = np.zeros((B, nc))
+            for ci, st in enumerate(range(0, Tn, b)):
+                n = min(b, Tn - st)
+                nxt = toks[:, st + n] if st + n < Tn else np.full(B, -1, np.int32)
+                losses[:, ci] = m.prefill_chunk(toks[:, st:st + n], nxt)
+        assert m.position == Tn
+        fw = [[m.fast_weights(q, i) for i in range(shape.n_trainable)] for q in range(B)]
+    finally:
+        m.close()
+    return losses, fw
+
+
+@pytest.mark.parametrize("name,n_seqs,api,concurrent", [
+    ("dh96_ahead4", 5, "sequence", True),   # five sequences on four lanes: the first lane takes two in turn
+    ("dh96_ahead4", 3, "sequence", False),  # one lane, the sequences one after another
+    ("dh64", 4, "chunk", True),              # per-chunk calls, every sequence on its own lane
+    ("fp32_dh64", 2, "sequence", True),
+])
+def test_several_sequences_match_the_oracle(name, n_seqs, api, concurrent):
+    s, toks = multi_sequence_case(name, n_seqs)
+    blob = weight_blob(s)
+    cfg = O.Config.from_shape(s)
+    P = O.unpack(blob, cfg)
+    losses, fw = run_gpu_multi(s, toks, blob, api, concurrent)
+    tl, tw = TOL[s.compute]
+    L, S = s.n_layers, s.n_trainable
+    for q in range(n_seqs):
+        ref_losses, Pf = O.run_sequence(cfg, P, toks[q], s.eta)
+        lr = np.abs(losses[q] - ref_losses) / np.abs(ref_losses)
+        print(f"\n{name} x{n_seqs} {api} seq {q}: loss rel err max {lr.max():.2e}")
+        assert lr.max() < tl, (q, losses[q], ref_losses)
+        for i in range(S):
+            l = L - S + i
+            for w, key in zip(fw[q][i], (f"W_up.{l}", f"W_down.{l}")):
+                assert rel(w, Pf[key]) < tw, (q, key)
+                assert rel(w - P[key], Pf[key] - P[key]) < DW_TOL[s.compute], (q, key)
