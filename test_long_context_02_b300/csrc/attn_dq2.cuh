@@ -119,7 +119,8 @@ TTT_DEV void dq2_body(const CUtensorMap* tQ, const CUtensorMap* tQl, const CUten
   uint64_t* ds_full = bars + 13;  // 2 (per score buffer)
   uint64_t* dq_full = bars + 15;  // 1
   uint64_t* drain = bars + 16;    // 1
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
+  uint64_t* dp_free = bars + 17;  // 1 (the softmax of the last tile has read dP out of TMEM)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const AttnArgs& g = a.g;
@@ -142,6 +143,7 @@ TTT_DEV void dq2_body(const CUtensorMap* tQ, const CUtensorMap* tQl, const CUten
     }
     mbar_init(dq_full, 1);
     mbar_init(drain, 1);
+    mbar_init(dp_free, 256);
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async();
@@ -236,11 +238,13 @@ TTT_DEV void dq2_body(const CUtensorMap* tQ, const CUtensorMap* tQl, const CUten
       }
       mma_commit_w(&k_empty[j % C::KST]);
     };
-    // Tensor-pipe order per key tile j: dP_j, dQ_{j-1}, S_{j+1}.  The softmax of tile j needs
-    // only S_j (issued a tile earlier) and dP_j, so it runs while dQ_{j-1} and S_{j+1}
-    // execute.  S_{j+1} overwrites the score buffer of dS_{j-1}, after dQ_{j-1} in issue
-    // order; K_{j+1} has a stage of its own (three key stages), so its load does not wait
-    // for dQ_{j-1} to release K_{j-1}.
+    // Tensor-pipe order per key tile j: dP_j, dQ_{j-1}, S_{j+1}.  dP_j goes into the one dP
+    // buffer as soon as the softmax of tile j-1 has loaded dP_{j-1} into registers (dp_free),
+    // so it executes during that softmax; the softmax of tile j then finds S_j (issued a
+    // tile earlier) and dP_j ready, and runs while dQ_{j-1} and S_{j+1} execute.  dQ_{j-1}
+    // waits for dS_{j-1} (ds_full).  S_{j+1} overwrites the score buffer of dS_{j-1}, after
+    // dQ_{j-1} in issue order; K_{j+1} has a stage of its own (three key stages), so its
+    // load does not wait for dQ_{j-1} to release K_{j-1}.
     bool ok = J > 0 && wait_all(q_full, 0) && wait_all(&k_full[0], 0);
     if (ok) {
       tc_fence_after();
@@ -252,8 +256,8 @@ TTT_DEV void dq2_body(const CUtensorMap* tQ, const CUtensorMap* tQl, const CUten
         ok = false;
         break;
       }
-      // the softmax of tile j-1 has read dP_{j-1} and written dS_{j-1}
-      if (j > 0 && !wait_all(&ds_full[s ^ 1], (uint32_t)(((j - 1) >> 1) & 1))) {
+      // the softmax of tile j-1 has read dP_{j-1} out of the dP buffer
+      if (j > 0 && !wait_all(dp_free, (uint32_t)((j - 1) & 1))) {
         ok = false;
         break;
       }
@@ -261,7 +265,14 @@ TTT_DEV void dq2_body(const CUtensorMap* tQ, const CUtensorMap* tQl, const CUten
       xk(tmem + T_DP, dob, smem_u32(smem + C::V_OFF + s * C::NOP * C::TILE));  // dP_j = dO V_j^T
       mma_commit_w(&s_full[s]);
       mma_commit_w(&v_empty[s]);
-      if (j > 0) dq_mma(j - 1);
+      if (j > 0) {  // dQ_{j-1} once the softmax of tile j-1 has written dS_{j-1}
+        if (!wait_all(&ds_full[s ^ 1], (uint32_t)(((j - 1) >> 1) & 1))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        dq_mma(j - 1);
+      }
       if (j + 1 < J) {  // S_{j+1} into the other score buffer
         if (!wait_all(&k_full[(j + 1) % C::KST], (uint32_t)(((j + 1) / C::KST) & 1))) {
           ok = false;
@@ -305,6 +316,8 @@ TTT_DEV void dq2_body(const CUtensorMap* tQ, const CUtensorMap* tQl, const CUten
       tc_fence_after();
       float sd[128];  // [0,64): S row, [64,128): dP row, under one wait
       tmem_ld64x2(trow + (uint32_t)(s * 128 + b0), trow + T_DP + (uint32_t)b0, sd);
+      tc_fence_before();
+      mbar_arrive(dp_free);  // the dP buffer may take dP_{j+1} now
       const float* sv = sd;
       const float* dp = sd + 64;
       uint32_t hi[32], lo[32];
