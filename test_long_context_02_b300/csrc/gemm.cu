@@ -739,7 +739,7 @@ int gemm_run(int epi, const Opnd& A, const Opnd& B, GemmArgs g, bool split, cuda
   int bn = pick_bn(g.M, g.N), ks = 1;
   if ((epi == EPI_F32 || epi == EPI_RESID) && g.allow_ksplit) choose_tiling(g.M, g.N, g.K, true, &bn, &ks);
   g.ksplit = ks;
-  if (ks > 1) {  // the slices add into out32: start it at 0 (F32) or at the residual (RESID)
+  if (ks > 1 && !g.out32_ready) {  // the slices add into out32: start it at 0 (F32) or at the residual (RESID)
     cudaError_t e;
     if (epi == EPI_F32)
       e = cudaMemset2DAsync(g.out32, (size_t)g.ldo32 * 4, 0, (size_t)g.N * 4, (size_t)g.M, st);

@@ -63,6 +63,9 @@ struct GemmArgs {
   // the sum order then varies from run to run.
   bool allow_ksplit = false;
   int ksplit = 1;  // set by gemm_run
+  // K slices: out32 already holds their start value (zero for F32, the residual for
+  // RESID), set by an earlier kernel, so gemm_run enqueues no clear or copy
+  bool out32_ready = false;
 };
 
 // One GEMM operand in HBM.  K-major: row-major [rows][ld] holding the K index

@@ -96,13 +96,15 @@ __global__ void targets_kernel(const int* __restrict__ tok, int n, const int* __
   tgt[i] = t;
 }
 
-// y = x * g / sqrt(mean(x^2) + eps) -> bf16 (hi, lo); rstd saved when requested.
+// y = x * g / sqrt(mean(x^2) + eps) -> bf16 (hi, lo); rstd saved when requested; x
+// also copied to x_copy when given (the start value of a K-sliced residual product).
 // One warp per row; lane l holds columns l*8 + 256*i (i < NCH) in registers, so
 // the row is read from HBM once and every load of the row is in flight at once.
 template <int NCH>
 __global__ void __launch_bounds__(128) rmsnorm_kernel(const float* __restrict__ x, const float* __restrict__ g,
                                                       float eps, int n, int d, bf16* __restrict__ yh,
-                                                      bf16* __restrict__ yl, float* __restrict__ rstd) {
+                                                      bf16* __restrict__ yl, float* __restrict__ rstd,
+                                                      float* __restrict__ x_copy) {
   pdl_wait();
   pdl_launch_dependents();
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
@@ -117,6 +119,17 @@ __global__ void __launch_bounds__(128) rmsnorm_kernel(const float* __restrict__ 
       load8(xr + c, v[i]);
 #pragma unroll
       for (int e = 0; e < 8; ++e) ss += v[i][e] * v[i][e];
+    }
+  }
+  if (x_copy) {
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+      const int c = lane * 8 + 256 * i;
+      if (c < d) {
+        float4* o = reinterpret_cast<float4*>(x_copy + (long)row * d + c);
+        o[0] = make_float4(v[i][0], v[i][1], v[i][2], v[i][3]);
+        o[1] = make_float4(v[i][4], v[i][5], v[i][6], v[i][7]);
+      }
     }
   }
   ss = warp_sum(ss);
@@ -136,12 +149,15 @@ __global__ void __launch_bounds__(128) rmsnorm_kernel(const float* __restrict__ 
 }
 
 // out = resid + [r g dy - x r^3/d * sum(dy g x)]  (gradient of RMSNorm w.r.t. its input, gain frozen)
-// Same register layout as the forward: dy and x of the row are read once.
+// Same register layout as the forward: dy and x of the row are read once.  With
+// clear_dy, dy's row is set to zero once read (the next K-sliced product into that
+// buffer adds onto zeros).
 template <int NCH>
-__global__ void __launch_bounds__(128) rmsnorm_bwd_kernel(const float* __restrict__ dy, const float* __restrict__ x,
+__global__ void __launch_bounds__(128) rmsnorm_bwd_kernel(const float* dy, const float* __restrict__ x,
                                                           const float* __restrict__ g, const float* __restrict__ rstd,
                                                           const float* resid, int n, int d, float* out,
-                                                          bf16* __restrict__ oh, bf16* __restrict__ ol) {
+                                                          bf16* __restrict__ oh, bf16* __restrict__ ol,
+                                                          float* clear_dy) {
   pdl_wait();
   pdl_launch_dependents();
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
@@ -165,6 +181,17 @@ __global__ void __launch_bounds__(128) rmsnorm_bwd_kernel(const float* __restric
       load8(g + c, gg);
 #pragma unroll
       for (int e = 0; e < 8; ++e) s += a[i][e] * gg[e] * b[i][e];
+    }
+  }
+  if (clear_dy) {  // each lane clears only the columns it has loaded
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+      const int c = lane * 8 + 256 * i;
+      if (c < d) {
+        float4* z = reinterpret_cast<float4*>(clear_dy + base + c);
+        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
   }
   s = warp_sum(s);
@@ -488,38 +515,42 @@ constexpr int kNormMaxChunks = 16;
 
 template <int NCH>
 int norm_fwd_n(const float* x, const float* g, float eps, int n, int d, bf16* yh, bf16* yl, float* rstd,
-               cudaStream_t st) {
+               float* x_copy, cudaStream_t st) {
   if constexpr (NCH > kNormMaxChunks) {
     return (int)cudaErrorInvalidValue;
   } else {
-    if ((d + 255) / 256 > NCH) return norm_fwd_n<NCH + 1>(x, g, eps, n, d, yh, yl, rstd, st);
-    return (int)launch_k(rmsnorm_kernel<NCH>, dim3((n + kNormWarps - 1) / kNormWarps), dim3(kNormWarps * 32), 0, st, x, g, eps, n, d, yh, yl, rstd);
+    if ((d + 255) / 256 > NCH) return norm_fwd_n<NCH + 1>(x, g, eps, n, d, yh, yl, rstd, x_copy, st);
+    return (int)launch_k(rmsnorm_kernel<NCH>, dim3((n + kNormWarps - 1) / kNormWarps), dim3(kNormWarps * 32), 0, st,
+                         x, g, eps, n, d, yh, yl, rstd, x_copy);
   }
 }
 
 template <int NCH>
 int norm_bwd_n(const float* dy, const float* x, const float* g, const float* rstd, const float* resid, int n, int d,
-               float* out, bf16* oh, bf16* ol, cudaStream_t st) {
+               float* out, bf16* oh, bf16* ol, float* clear_dy, cudaStream_t st) {
   if constexpr (NCH > kNormMaxChunks) {
     return (int)cudaErrorInvalidValue;
   } else {
-    if ((d + 255) / 256 > NCH) return norm_bwd_n<NCH + 1>(dy, x, g, rstd, resid, n, d, out, oh, ol, st);
-    return (int)launch_k(rmsnorm_bwd_kernel<NCH>, dim3((n + kNormWarps - 1) / kNormWarps), dim3(kNormWarps * 32), 0, st, dy, x, g, rstd, resid, n, d, out, oh, ol);
+    if ((d + 255) / 256 > NCH) return norm_bwd_n<NCH + 1>(dy, x, g, rstd, resid, n, d, out, oh, ol, clear_dy, st);
+    return (int)launch_k(rmsnorm_bwd_kernel<NCH>, dim3((n + kNormWarps - 1) / kNormWarps), dim3(kNormWarps * 32), 0,
+                         st, dy, x, g, rstd, resid, n, d, out, oh, ol, clear_dy);
   }
 }
 
 int rows_rmsnorm(const float* x, const float* g, float eps, int n, int d, bf16* yh, bf16* yl, float* rstd,
-                 cudaStream_t st) {
+                 cudaStream_t st, float* x_copy) {
   if (n <= 0) return 0;
-  if (d % 8) return (int)cudaErrorInvalidValue;
-  return norm_fwd_n<1>(x, g, eps, n, d, yh, yl, rstd, st);
+  if (d % 8 || x_copy == x) return (int)cudaErrorInvalidValue;
+  return norm_fwd_n<1>(x, g, eps, n, d, yh, yl, rstd, x_copy, st);
 }
 
 int rows_rmsnorm_bwd(const float* dy, const float* x, const float* g, const float* rstd, const float* resid, int n,
-                     int d, float* out, bf16* oh, bf16* ol, cudaStream_t st) {
+                     int d, float* out, bf16* oh, bf16* ol, cudaStream_t st, bool clear_dy) {
   if (n <= 0) return 0;
   if (d % 8) return (int)cudaErrorInvalidValue;
-  return norm_bwd_n<1>(dy, x, g, rstd, resid, n, d, out, oh, ol, st);
+  // clearing dy must not touch a buffer the kernel reads or writes elsewhere
+  if (clear_dy && (dy == x || dy == resid || dy == out)) return (int)cudaErrorInvalidValue;
+  return norm_bwd_n<1>(dy, x, g, rstd, resid, n, d, out, oh, ol, clear_dy ? const_cast<float*>(dy) : nullptr, st);
 }
 
 int rows_rope_table(long pos0, int n, int dh, const double* inv_freq, float* cs, float* sn, cudaStream_t st) {

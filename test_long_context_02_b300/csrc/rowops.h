@@ -6,10 +6,12 @@ namespace ttt {
 
 int rows_embed(const int* tok, int n, const float* E, int V, int d, float* x, int* err, cudaStream_t st);
 int rows_targets(const int* tok, int n, const int* next, int V, int* tgt, int* err, cudaStream_t st);
+// x_copy (optional, not x): also receives x, the start value of a K-sliced residual product
 int rows_rmsnorm(const float* x, const float* g, float eps, int n, int d, bf16* yh, bf16* yl, float* rstd,
-                 cudaStream_t st);
+                 cudaStream_t st, float* x_copy = nullptr);
+// clear_dy: dy is set to zero once read (dy must be none of x, resid, out)
 int rows_rmsnorm_bwd(const float* dy, const float* x, const float* g, const float* rstd, const float* resid, int n,
-                     int d, float* out, bf16* oh, bf16* ol, cudaStream_t st);
+                     int d, float* out, bf16* oh, bf16* ol, cudaStream_t st, bool clear_dy = false);
 int rows_rope_table(long pos0, int n, int dh, const double* inv_freq, float* cs, float* sn, cudaStream_t st);
 int rows_rope_qkv(const float* qkv, const float* cs, const float* sn, int n, int H, int dh, bf16* qh, bf16* ql,
                   bf16* kh, bf16* kl, bf16* vh, bf16* vl, cudaStream_t st);

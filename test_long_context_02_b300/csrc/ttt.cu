@@ -296,9 +296,11 @@ int layer_forward(ttt_ctx* c, Lane& ln, Seq& sq_, int l, int si, bool save, int 
   Pair ko0 = ln.kown.at((long)l * R * d), vo0 = ln.vown.at((long)l * R * d);
   Pair kr = sq_.ring_k.at((long)l * k * d), vr = sq_.ring_v.at((long)l * k * d);
 
-  RUN(K_RMSNORM, 1, 0, 0, nn * dd * (4 + eb),
+  // with a separate output buffer, the norm also copies its input there: the start value
+  // of the O product's K slices (x + o.Wo), so the product needs no copy of its own
+  RUN(K_RMSNORM, 1, 0, 0, nn * dd * (4 + eb + (hbuf != xin ? 4 : 0)),
       rows_rmsnorm(xin, c->gains + (long)(2 * l) * d, c->cfg.rms_eps, n, d, xn_a.hi, xn_a.lo,
-                   suf ? ln.srs_a + (long)si * b : nullptr, st));
+                   suf ? ln.srs_a + (long)si * b : nullptr, st, hbuf != xin ? hbuf : nullptr));
   Pair qw = q0.at(ro), kw = ko0.at(ro), vw = vo0.at(ro);
   if (qkv_rope_bn(dh, d, sp)) {  // RoPE and the q / own k / own v writes fused into the product's epilogue
     GemmArgs g;
@@ -333,12 +335,13 @@ int layer_forward(ttt_ctx* c, Lane& ln, Seq& sq_, int l, int si, bool save, int 
     GemmArgs g;
     g.M = n; g.N = d; g.K = d;
     g.out32 = hbuf; g.ldo32 = d; g.resid = xin; g.ldr = d; g.err = c->derr; g.allow_ksplit = true;
+    g.out32_ready = hbuf != xin;  // holds xin (the norm above copied it)
     RUN(K_GEMM_O, 1, 2 * nn * dd * dd, 2 * nn * dd * dd * ops, 0,
         gemm_run(EPI_RESID, opnd(o0.at(ro), d, 0), opnd(c->Wo.at((long)l * d * d), d, 1), g, sp, st));
   }
-  RUN(K_RMSNORM, 1, 0, 0, nn * dd * (4 + eb),
+  RUN(K_RMSNORM, 1, 0, 0, nn * dd * (4 + eb + (xout != hbuf ? 4 : 0)),
       rows_rmsnorm(hbuf, c->gains + (long)(2 * l + 1) * d, c->cfg.rms_eps, n, d, xn_m.hi, xn_m.lo,
-                   suf ? ln.srs_m + (long)si * b : nullptr, st));
+                   suf ? ln.srs_m + (long)si * b : nullptr, st, xout != hbuf ? xout : nullptr));
   {
     GemmArgs g;
     g.M = n; g.N = f; g.K = d;
@@ -352,6 +355,7 @@ int layer_forward(ttt_ctx* c, Lane& ln, Seq& sq_, int l, int si, bool save, int 
     GemmArgs g;
     g.M = n; g.N = d; g.K = f;
     g.out32 = xout; g.ldo32 = d; g.resid = hbuf; g.ldr = d; g.err = c->derr; g.allow_ksplit = true;
+    g.out32_ready = xout != hbuf;  // holds h (the norm above copied it)
     Pair w = fast ? sq_.down16.at((long)si * f * d) : c->Wdown.at((long)l * f * d);
     RUN(K_GEMM_DOWN, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 0,
         gemm_run(EPI_RESID, opnd(ub, f, 0), opnd(w, d, 1), g, sp, st));
@@ -466,12 +470,13 @@ int suffix_step(ttt_ctx* c, Lane& ln, int s, int row, const int* tok, int n, con
     GemmArgs g;
     g.M = n; g.N = d; g.K = V;
     g.out32 = ln.dxn; g.ldo32 = d; g.err = c->derr; g.allow_ksplit = true;
+    g.out32_ready = true;  // dxn is zero between its uses (each reader clears it)
     RUN(K_LM_DX, 1, 2 * nn * dd * VV, 2 * nn * dd * VV * ops, 0,
         gemm_run(EPI_F32, opnd(ln.dz, V, 0), opnd(c->Wlm, V, 0), g, sp, st));
   }
   RUN(K_RMSNORM, 1, 0, 0, nn * dd * (12 + eb),
       rows_rmsnorm_bwd(ln.dxn, ln.x, c->gains + (long)(2 * L) * d, ln.rs_f, nullptr, n, d, ln.dy, ln.dy16.hi,
-                       ln.dy16.lo, st));
+                       ln.dy16.lo, st, true));
   // The dW + SGD products go to the third stream when it is free to run beside the rest:
   //   W_down step after dA (which reads W_down and dY)      -> before dY is overwritten
   //   W_up step after dXn (which reads W_up) and dA        -> before dA is overwritten
@@ -514,6 +519,7 @@ int suffix_step(ttt_ctx* c, Lane& ln, int s, int row, const int* tok, int n, con
       GemmArgs g;
       g.M = n; g.N = d; g.K = f;
       g.out32 = ln.dxn; g.ldo32 = d; g.err = c->derr; g.allow_ksplit = true;
+      g.out32_ready = true;
       RUN(K_MLP_DX, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 0,
           gemm_run(EPI_F32, opnd(ln.da, f, 0), opnd(up16, f, 0), g, sp, st));
     }
@@ -550,7 +556,7 @@ int suffix_step(ttt_ctx* c, Lane& ln, int s, int row, const int* tok, int n, con
     // dH = dY + RMSNorm_m^T(dXn_m)
     RUN(K_RMSNORM, 1, 0, 0, nn * dd * (20 + eb),
         rows_rmsnorm_bwd(ln.dxn, ln.sh + (long)si * b * d, c->gains + (long)(2 * l + 1) * d,
-                         ln.srs_m + (long)si * b, ln.dy, n, d, ln.dh32, ln.dh16.hi, ln.dh16.lo, st));
+                         ln.srs_m + (long)si * b, ln.dy, n, d, ln.dh32, ln.dh16.hi, ln.dh16.lo, st, true));
     {  // dO = dH Wo^T
       GemmArgs g;
       g.M = n; g.N = d; g.K = d;
@@ -591,6 +597,7 @@ int suffix_step(ttt_ctx* c, Lane& ln, int s, int row, const int* tok, int n, con
       GemmArgs g;
       g.M = n; g.N = d; g.K = 3 * d;
       g.out32 = ln.dxn; g.ldo32 = d; g.err = c->derr; g.allow_ksplit = true;
+      g.out32_ready = true;
       RUN(K_ATTN_DX, 1, 6 * nn * dd * dd, 6 * nn * dd * dd * ops, 0,
           gemm_run(EPI_F32, opnd(ln.dqkv, 3 * d, 0), opnd(c->Wqkv.at((long)l * d * 3 * d), 3 * d, 0), g, sp, st));
     }
@@ -601,7 +608,7 @@ int suffix_step(ttt_ctx* c, Lane& ln, int s, int row, const int* tok, int n, con
     // dY_{l-1} = dH + RMSNorm_a^T(dXn_a)
     RUN(K_RMSNORM, 1, 0, 0, nn * dd * (20 + eb),
         rows_rmsnorm_bwd(ln.dxn, ln.sx + (long)si * b * d, c->gains + (long)(2 * l) * d, ln.srs_a + (long)si * b,
-                         ln.dh32, n, d, ln.dy, ln.dy16.hi, ln.dy16.lo, st));
+                         ln.dh32, n, d, ln.dy, ln.dy16.hi, ln.dy16.lo, st, true));
   }
   if (side) {  // every step of this chunk is in place before anything later reads the weights
     CK(cudaStreamWaitEvent(st, ln.ev_wd, 0));
@@ -872,6 +879,9 @@ extern "C" int ttt_load_weights(ttt_ctx* c, const float* blob, size_t n_floats) 
         CK(cudaMemsetAsync(s.ring_v.lo, 0, rb, st));
       }
     }
+    // the K-sliced dX products add into dxn, which its readers leave at zero; a chunk cut
+    // short by an error may not have, so start from zero
+    for (Lane& ln : c->lanes) CK(cudaMemsetAsync(ln.dxn, 0, (size_t)c->b * d * sizeof(float), st));
     CK(cudaMemsetAsync(c->derr, 0, sizeof(int), st));
     CK(cudaStreamSynchronize(st));
     return TTT_OK;
