@@ -262,6 +262,14 @@ typedef struct {
   double bytes;
 } ttt_kernel_stat;
 TTT_API int ttt_profile(ttt_ctx* ctx, int64_t class_mask);
+/*
+ * Bracket only one launch in `every` (>= 1; 1, the default, brackets all) of
+ * each profiled class, counted in issue order from the next ttt_profile call.
+ * An event between two launches ends the overlap of programmatic dependent
+ * launch there, so sampling keeps the timed work closer to an unprofiled run.
+ * Returns TTT_ERR_ARG for every < 1.
+ */
+TTT_API int ttt_profile_sample(ttt_ctx* ctx, int32_t every);
 /* Name of kernel class `cls` (0-based), NULL past the last class. */
 TTT_API const char* ttt_profile_class_name(int cls);
 TTT_API int ttt_profile_read(ttt_ctx* ctx, ttt_kernel_stat* out, int max_out, int* n_out);

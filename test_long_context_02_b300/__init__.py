@@ -144,6 +144,7 @@ class ttt_kernel_stat(ctypes.Structure):
 
 
 ttt_profile = _sig("ttt_profile", ctypes.c_int, _vp, _i64)
+ttt_profile_sample = _sig("ttt_profile_sample", ctypes.c_int, _vp, _i32)
 ttt_profile_class_name = _sig("ttt_profile_class_name", ctypes.c_char_p, ctypes.c_int)
 
 
@@ -312,13 +313,15 @@ class TTT:
     def launches(self) -> int:
         return int(ttt_launch_count(self._h))
 
-    def profile(self, enable=True, classes=None):
-        """Start (enable) or stop event timing; `classes` limits it to those class names."""
+    def profile(self, enable=True, classes=None, every=1):
+        """Start (enable) or stop event timing; `classes` limits it to those class names,
+        `every` to one launch in that many of each class."""
         mask = 0
         if enable:
             names = profile_classes()
             mask = -1 if classes is None else sum(1 << names.index(c) for c in classes)
         self._check(ttt_profile(self._h, mask), "ttt_profile")
+        self._check(ttt_profile_sample(self._h, every), "ttt_profile_sample")
 
     def profile_read(self):
         """{class name: dict(launches, ms, alg_flops, exec_flops, bytes)} since ttt_profile(1)."""

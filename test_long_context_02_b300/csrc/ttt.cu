@@ -19,10 +19,12 @@
 //              dU = dY W_down^T (x GELU'), dW_down = U^T dY with the SGD step in
 //              its epilogue, dXn = dA W_up^T, dW_up = Xn^T dA with the SGD step,
 //              then (except for the first trainable block) RMSNorm backward,
-//              dO = dH Wo^T, attention backward, RoPE backward, dXn = dQKV Wqkv^T,
-//              RMSNorm backward.  Every dX product reads the weights before the
-//              step (it runs first on the stream); all gradients of the step are
-//              taken at the chunk's starting weights.
+//              dO = dH Wo^T, attention backward (which writes dQKV with RoPE's
+//              rotation transposed), dXn = dQKV Wqkv^T, RMSNorm backward.  The
+//              dW + SGD products run on the lane's third stream; every dX
+//              product reads the weights before the step (the events order it
+//              first); all gradients of the step are taken at the chunk's
+//              starting weights.
 //   commit   : the chunk's keys/values of every layer go into the window cache.
 #include <cmath>
 #include <cstdio>
@@ -123,6 +125,8 @@ struct ttt_ctx {
   // launch counting and optional per-class event timing
   int64_t launches = 0;
   uint64_t prof_mask = 0;   // bit i: bracket launches of kernel class i with events
+  int prof_every = 1;       // ... one launch in prof_every of each such class
+  int64_t prof_seen[64] = {};
   std::vector<cudaEvent_t> ev_pool;
   size_t ev_used = 0;
   struct ProfRec {
@@ -232,7 +236,8 @@ cudaEvent_t next_event(ttt_ctx* c) {
 template <class F>
 int site(ttt_ctx* c, int cls, cudaStream_t sst, int nkern, double alg, double exec, double bytes, F&& f) {
   cudaEvent_t a = nullptr;
-  if (((c->prof_mask >> cls) & 1u) && (a = next_event(c))) cudaEventRecord(a, sst);
+  if (((c->prof_mask >> cls) & 1u) && c->prof_seen[cls]++ % c->prof_every == 0 && (a = next_event(c)))
+    cudaEventRecord(a, sst);
   const int r = f();
   if (a) {
     cudaEvent_t b = next_event(c);
@@ -1333,7 +1338,15 @@ extern "C" int ttt_profile(ttt_ctx* c, int64_t class_mask) {
   c->recs.clear();
   c->ev_used = 0;
   for (auto& a : c->acc) a = ttt_ctx::ProfAcc();
+  for (auto& n : c->prof_seen) n = 0;
   c->prof_mask = (uint64_t)class_mask & ((1ull << K_NCLS) - 1);
+  return TTT_OK;
+}
+
+extern "C" int ttt_profile_sample(ttt_ctx* c, int32_t every) {
+  if (!c || every < 1) return TTT_ERR_ARG;
+  c->prof_every = every;
+  for (auto& n : c->prof_seen) n = 0;
   return TTT_OK;
 }
 

@@ -146,6 +146,7 @@ def test_context_calls_reject_null_context():
     assert T.ttt_launch_count(None) == -1
     assert T.ttt_state_bytes(None) == -1
     assert T.ttt_set_concurrency(None, 1) == T.TTT_ERR_ARG
+    assert T.ttt_profile_sample(None, 8) == T.TTT_ERR_ARG
     assert T.ttt_export_state(None, 0, 1, 48) == T.TTT_ERR_ARG
     assert T.ttt_import_state(None, 0, 1, 48) == T.TTT_ERR_ARG
     assert T.ttt_position(None) == -1
