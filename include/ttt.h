@@ -49,7 +49,7 @@ extern "C" {
 
 #define TTT_OK 0
 #define TTT_ERR_ARG (-1)         /* null pointer, n outside 1..b, token id outside [0, vocab), k < b, ... */
-#define TTT_ERR_UNSUPPORTED (-2) /* a shape this build does not handle (see ttt_create)                 */
+#define TTT_ERR_UNSUPPORTED (-2) /* a shape the library does not handle (see ttt_create)                */
 #define TTT_ERR_STATE (-3)       /* prefill before ttt_load_weights                                     */
 #define TTT_ERR_OOM (-4)         /* device allocation failed                                            */
 #define TTT_ERR_CUDA (-5)        /* a CUDA runtime call failed                                          */
