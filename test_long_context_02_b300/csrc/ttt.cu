@@ -79,7 +79,7 @@ struct Lane {
   // the fast-weight gradient products with their SGD step run on a third stream beside
   // the rest of the chunk's backward (nothing in it reads the updated weights)
   cudaStream_t st3 = nullptr;
-  cudaEvent_t ev_da = nullptr, ev_dx = nullptr, ev_wd = nullptr, ev_wu = nullptr;
+  cudaEvent_t ev_dx = nullptr, ev_wu = nullptr;
   Pair kown, vown;           // [L][R][d]
   float *sx = nullptr, *sh = nullptr, *srs_a = nullptr, *srs_m = nullptr, *slse = nullptr, *sa = nullptr;
   Pair sq, so, sxm, su;
@@ -482,20 +482,17 @@ int suffix_step(ttt_ctx* c, Lane& ln, int s, int row, const int* tok, int n, con
   RUN(K_RMSNORM, 1, 0, 0, nn * dd * (12 + eb),
       rows_rmsnorm_bwd(ln.dxn, ln.x, c->gains + (long)(2 * L) * d, ln.rs_f, nullptr, n, d, ln.dy, ln.dy16.hi,
                        ln.dy16.lo, st, true));
-  // The dW + SGD products go to the third stream when it is free to run beside the rest:
-  //   W_down step after dA (which reads W_down and dY)      -> before dY is overwritten
-  //   W_up step after dXn (which reads W_up) and dA        -> before dA is overwritten
-  //   all steps done before the chunk ends (the next chunk's forward reads the weights).
+  // The block's two dW + SGD products go to the third stream, after dXn (the last product
+  // that reads the old W_up; dA read the old W_down before it), behind one event; one
+  // wait brings them back before dY is overwritten (they read dY and dA), and a last one
+  // before the commit (the next chunk's forward reads the weights).  Fewer stream
+  // operations between the chain's kernels keep more launch overlap.
   const bool side = ln.st3 != nullptr && c->concurrent;
   cudaStream_t sw = side ? ln.st3 : st;
-  bool wd_pending = false, wu_pending = false;
+  bool steps_pending = false;
   for (int si = S - 1; si >= 0; --si) {
     const int l = P0 + si;
     Pair up16 = sq_.up16.at((long)si * d * f), down16 = sq_.down16.at((long)si * f * d);
-    if (wu_pending) {  // the previous block's W_up step has read dA
-      CK(cudaStreamWaitEvent(st, ln.ev_wu, 0));
-      wu_pending = false;
-    }
     {  // dA = (dY W_down^T) * gelu'(a)
       GemmArgs g;
       g.M = n; g.N = f; g.K = d;
@@ -503,22 +500,6 @@ int suffix_step(ttt_ctx* c, Lane& ln, int s, int row, const int* tok, int n, con
       g.oh = ln.da.hi; g.ol = ln.da.lo; g.ldo = f; g.err = c->derr;
       RUN(K_MLP_DX, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 0,
           gemm_run(EPI_GELU_BWD, opnd(ln.dy16, d, 0), opnd(down16, d, 0), g, sp, st));
-    }
-    {  // W_down -= eta U^T dY
-      if (side) {
-        CK(cudaEventRecord(ln.ev_da, st));
-        CK(cudaStreamWaitEvent(sw, ln.ev_da, 0));
-      }
-      GemmArgs g;
-      g.M = f; g.N = d; g.K = n;
-      g.w32 = sq_.down32 + (long)si * f * d; g.wh = down16.hi; g.wl = down16.lo; g.ldw = d; g.eta = eta;
-      g.err = c->derr;
-      RUN_ON(sw, K_DW_SGD, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 8 * dd * ff,
-             gemm_run(EPI_SGD, opnd(ln.su.at((long)si * b * f), f, 1), opnd(ln.dy16, d, 1), g, sp, sw));
-      if (side) {
-        CK(cudaEventRecord(ln.ev_wd, sw));
-        wd_pending = true;
-      }
     }
     if (si > 0) {  // dXn_m = dA W_up^T  (before W_up changes)
       GemmArgs g;
@@ -541,21 +522,29 @@ int suffix_step(ttt_ctx* c, Lane& ln, int s, int row, const int* tok, int n, con
       RUN(K_MLP_DX, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 0,
           gemm_run(EPI_RESID, opnd(ln.da_s, f, 0), opnd(c->Wup_s.at((long)si * d * f), f, 0), g2, sp, st));
     }
+    if (side) {
+      CK(cudaEventRecord(ln.ev_dx, st));
+      CK(cudaStreamWaitEvent(sw, ln.ev_dx, 0));
+    }
+    {  // W_down -= eta U^T dY
+      GemmArgs g;
+      g.M = f; g.N = d; g.K = n;
+      g.w32 = sq_.down32 + (long)si * f * d; g.wh = down16.hi; g.wl = down16.lo; g.ldw = d; g.eta = eta;
+      g.err = c->derr;
+      RUN_ON(sw, K_DW_SGD, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 8 * dd * ff,
+             gemm_run(EPI_SGD, opnd(ln.su.at((long)si * b * f), f, 1), opnd(ln.dy16, d, 1), g, sp, sw));
+    }
     {  // W_up -= eta Xn_m^T dA
-      if (side) {
-        CK(cudaEventRecord(ln.ev_dx, st));
-        CK(cudaStreamWaitEvent(sw, ln.ev_dx, 0));
-      }
       GemmArgs g;
       g.M = d; g.N = f; g.K = n;
       g.w32 = sq_.up32 + (long)si * d * f; g.wh = up16.hi; g.wl = up16.lo; g.ldw = f; g.eta = eta;
       g.err = c->derr;
       RUN_ON(sw, K_DW_SGD, 1, 2 * nn * dd * ff, 2 * nn * dd * ff * ops, 8 * dd * ff,
              gemm_run(EPI_SGD, opnd(ln.sxm.at((long)si * b * d), d, 1), opnd(ln.da, f, 1), g, sp, sw));
-      if (side) {
-        CK(cudaEventRecord(ln.ev_wu, sw));
-        wu_pending = true;
-      }
+    }
+    if (side) {
+      CK(cudaEventRecord(ln.ev_wu, sw));
+      steps_pending = true;
     }
     if (si == 0) break;  // the first trainable block's attention needs no gradient
     // dH = dY + RMSNorm_m^T(dXn_m)
@@ -606,19 +595,16 @@ int suffix_step(ttt_ctx* c, Lane& ln, int s, int row, const int* tok, int n, con
       RUN(K_ATTN_DX, 1, 6 * nn * dd * dd, 6 * nn * dd * dd * ops, 0,
           gemm_run(EPI_F32, opnd(ln.dqkv, 3 * d, 0), opnd(c->Wqkv.at((long)l * d * 3 * d), 3 * d, 0), g, sp, st));
     }
-    if (wd_pending) {  // the W_down step has read dY
-      CK(cudaStreamWaitEvent(st, ln.ev_wd, 0));
-      wd_pending = false;
+    if (steps_pending) {  // the block's steps have read dY and dA
+      CK(cudaStreamWaitEvent(st, ln.ev_wu, 0));
+      steps_pending = false;
     }
     // dY_{l-1} = dH + RMSNorm_a^T(dXn_a)
     RUN(K_RMSNORM, 1, 0, 0, nn * dd * (20 + eb),
         rows_rmsnorm_bwd(ln.dxn, ln.sx + (long)si * b * d, c->gains + (long)(2 * l) * d, ln.srs_a + (long)si * b,
                          ln.dh32, n, d, ln.dy, ln.dy16.hi, ln.dy16.lo, st, true));
   }
-  if (side) {  // every step of this chunk is in place before anything later reads the weights
-    CK(cudaStreamWaitEvent(st, ln.ev_wd, 0));
-    CK(cudaStreamWaitEvent(st, ln.ev_wu, 0));
-  }
+  if (steps_pending) CK(cudaStreamWaitEvent(st, ln.ev_wu, 0));  // every step is in place before the weights are read
   // ------------------------------------------------------------------- commit
   const double cb = (double)S * nn * dd * 2 * 2;
   const long os = (long)R * d, rs = (long)k * d;
@@ -765,7 +751,7 @@ extern "C" int ttt_create(const ttt_config* cfg, void* cuda_stream, ttt_ctx** ou
       made = mk_st(&ln.st);
       ln.own_st = made;
     }
-    made = made && mk_st(&ln.st2) && mk_st(&ln.st3) && mk_ev(&ln.ev_da) && mk_ev(&ln.ev_dx) && mk_ev(&ln.ev_wd) &&
+    made = made && mk_st(&ln.st2) && mk_st(&ln.st3) && mk_ev(&ln.ev_dx) &&
            mk_ev(&ln.ev_wu) && mk_ev(&ln.ev_fork) && mk_ev(&ln.ev_join) && mk_ev(&ln.ev_pass[0]) &&
            mk_ev(&ln.ev_pass[1]) && mk_ev(&ln.ev_suf[0]) && mk_ev(&ln.ev_suf[1]);
   }
@@ -797,8 +783,8 @@ extern "C" void ttt_destroy(ttt_ctx* c) {
   for (Lane& ln : c->lanes) {
     for (cudaStream_t t : {ln.own_st ? ln.st : nullptr, ln.st2, ln.st3})
       if (t) cudaStreamDestroy(t);
-    for (cudaEvent_t e : {ln.ev_fork, ln.ev_join, ln.ev_pass[0], ln.ev_pass[1], ln.ev_suf[0], ln.ev_suf[1], ln.ev_da,
-                          ln.ev_dx, ln.ev_wd, ln.ev_wu})
+    for (cudaEvent_t e : {ln.ev_fork, ln.ev_join, ln.ev_pass[0], ln.ev_pass[1], ln.ev_suf[0], ln.ev_suf[1],
+                          ln.ev_dx, ln.ev_wu})
       if (e) cudaEventDestroy(e);
   }
   if (c->ev_fork) cudaEventDestroy(c->ev_fork);
