@@ -175,6 +175,16 @@ def attn_fwd_traffic(shape, nc):
     return (passes * t["pass"] + steps * t["step"]) / (passes + steps)
 
 
+def chunk_major(tokens, b):
+    """Inputs of ttt_prefill_chunk for every chunk of tokens [B][T]: the ids of chunk c
+    as one [B][n_c] block after those of chunk c-1, and next[c][q], the token after
+    chunk c of sequence q (-1 after the last)."""
+    B, Tn = tokens.shape
+    ids = np.concatenate([tokens[:, s:s + b].reshape(-1) for s in range(0, Tn, b)]).astype(np.int32)
+    nxt = np.array([[tokens[q, s + b] if s + b < Tn else -1 for q in range(B)] for s in range(0, Tn, b)], np.int32)
+    return ids, nxt
+
+
 def workload_name(s):
     return (f"{s.n_layers}L d{s.d_model} H{s.n_heads} f{s.d_ff} V{s.vocab} k{s.window} b{s.chunk} "
             f"theta{s.rope_theta:g} eta{s.eta:g} {s.compute}: {s.n_seqs} x {s.seq_len} tokens")
@@ -301,9 +311,8 @@ def run_ours(a):
     e2e_steps = max(1, min(a.steps, 2))
     pin_tok = torch.tensor(tokens, dtype=torch.int32).pin_memory()
     # the per-chunk call takes [B][n] tokens of one chunk: the same ids, laid out chunk-major
-    chunk_major = np.concatenate([tokens[:, s:s + b].reshape(-1) for s in range(0, Tn, b)])
-    pin_ctok = torch.tensor(chunk_major, dtype=torch.int32).pin_memory()
-    nxt = np.array([[tokens[q, s + b] if s + b < Tn else -1 for q in range(B)] for s in range(0, Tn, b)], np.int32)
+    ctok, nxt = chunk_major(tokens, b)
+    pin_ctok = torch.tensor(ctok, dtype=torch.int32).pin_memory()
     pin_next = torch.tensor(nxt).pin_memory()
     pin_loss = torch.zeros((B, nc), dtype=torch.float32).pin_memory()
     pin_closs = torch.zeros((nc, B), dtype=torch.float32).pin_memory()

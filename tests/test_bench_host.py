@@ -53,3 +53,19 @@ def test_reference_sample_is_a_power_of_two_within_the_budget(steps, warmup, wan
     assert n & (n - 1) == 0 and 64 <= n <= 1024
     # more samples never get a larger sample
     assert bench.reference_tokens(steps + 10, warmup) <= n
+
+
+@pytest.mark.parametrize("B,T,b", [(1, 10, 4), (4, 12, 4), (3, 7, 8), (2, 9, 3)])
+def test_per_chunk_inputs_walk_every_sequence_chunk_by_chunk(B, T, b):
+    import numpy as np
+    tokens = np.arange(B * T, dtype=np.int32).reshape(B, T) + 100
+    ids, nxt = bench.chunk_major(tokens, b)
+    assert ids.size == B * T and nxt.shape == (-(-T // b), B)
+    off = 0
+    for c, s in enumerate(range(0, T, b)):
+        n = min(b, T - s)
+        block = ids[off:off + B * n].reshape(B, n)  # what one ttt_prefill_chunk call reads
+        off += B * n
+        assert (block == tokens[:, s:s + n]).all()
+        for q in range(B):
+            assert nxt[c, q] == (tokens[q, s + n] if s + n < T else -1)
